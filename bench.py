@@ -1,0 +1,447 @@
+"""Benchmark of the fused compressed optimizer step (FlashAdamW) on GB300.
+
+Default workload: the Llama-3.1-8B parameter table (291 tensors, 8.03e9
+parameters, BF16 theta' + INT8 rho + INT8 m + UINT8 v, FP16 group scales),
+one fused FlashAdamW step per iteration over the whole table -- one kernel
+launch of the library per step. Inputs are seeded synthetic tensors drawn on
+the device; nothing is skipped inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+("replicas only": the step has no exchange), the timed region is bracketed by
+barriers, the time is the maximum over ranks and rank 0 prints one JSON line.
+``--impl reference`` times the CPU oracle (plain scalar C) on the host cores
+over a bounded sample of the same workload and prints the same line.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FlashAdamW step params/s and achieved HBM GB/s vs ~8 TB/s (1xGB300)"
+UNIT = "params/s"
+# bytes one FlashAdamW step must move per parameter (each byte once):
+# read grad 2 + theta' 2 + rho 1 + m 1 + v 1 + 2 FP16 scales / 32, write all but grad
+ALGO_BYTES_PER_PARAM = {8: 12.25, 16: 14.25}
+FALLBACK_HBM_GBS = 6800.0
+CPU_SAMPLE_ROWS = ("layers.0.input_layernorm.weight", "layers.0.post_attention_layernorm.weight",
+                   "layers.0.self_attn.q_proj.weight", "layers.0.self_attn.k_proj.weight",
+                   "layers.0.self_attn.v_proj.weight", "layers.0.self_attn.o_proj.weight")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default="llama31_8b")
+    p.add_argument("--rho-bits", type=int, default=8, choices=(8, 16))
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="time budget of the CPU oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args(argv)
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _config(w, rho_bits, n_gpus):
+    return {
+        "workload": f"{w.name}: {len(w.params)} tensors, {w.numel} params, Flash{w.optimizer}"
+                    f" step (BF16 theta' + INT{rho_bits} rho + INT8 m"
+                    f"{' + UINT8 v' if w.optimizer == 'adamw' else ''}, G=32 FP16 scales)",
+        "params": w.numel,
+        "tensors": len(w.params),
+        "optimizer": w.optimizer,
+        "rho_bits": rho_bits,
+        "hparams": w.hparams,
+        "algorithmic_bytes_per_param": _algo_bytes(w, rho_bits),
+        "l2": "inputs larger than L2 (each step streams ~%.0f GB)" % (w.numel * _algo_bytes(w, rho_bits) / 1e9),
+        "grads": "one seeded synthetic BF16 gradient set, reused every step",
+        "parallelism": "replicas" if n_gpus > 1 else "single GPU",
+    }
+
+
+def _algo_bytes(w, rho_bits):
+    if w.optimizer == "adamw":
+        return ALGO_BYTES_PER_PARAM[rho_bits]
+    return 2 * (2 + rho_bits // 8 + 1 + 2 / 32) + 2
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (the cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OracleSample:
+    """Host state of a few rows of the workload, cut into group-aligned chunks
+    that the oracle steps on parallel threads (the oracle itself is untouched)."""
+
+    def __init__(self, w, rho_bits, chunk=1 << 20):
+        import numpy as np
+        import oracle
+        from quantized_optimizer_state_gb300 import workloads as wl
+        self.w = w
+        names = {p.name: i for i, p in enumerate(w.params)}
+        rows = [names[n] for n in CPU_SAMPLE_ROWS if n in names] or [0]
+        self.states, self.grads, self.chunks = [], [], []
+        with_v = w.optimizer == "adamw"
+        for i in rows:
+            p = w.params[i]
+            st = oracle.State.from_fp32(wl.init_weight(p, i), rho_bits, with_v,
+                                        w.hparams["weight_decay"])
+            g = wl.grad_bf16(w.grad, w.grad_scale, p.numel, i, 1)
+            self.states.append(st)
+            self.grads.append(g)
+            for lo in range(0, p.numel, chunk):
+                hi = min(p.numel, lo + chunk)
+                g0, g1 = lo // 32, (hi + 31) // 32
+                sub = oracle.State(st.theta_p[lo:hi], st.rho[lo:hi], st.m_q[lo:hi], st.m_scale[g0:g1],
+                                   None if st.v_q is None else st.v_q[lo:hi],
+                                   None if st.v_scale is None else st.v_scale[g0:g1],
+                                   st.weight_decay, rho_bits)
+                self.chunks.append((sub, np.ascontiguousarray(g[lo:hi])))
+        self.params = sum(s.numel for s in self.states)
+        self.threads = _cpu_threads()
+        self.pool = cf.ThreadPoolExecutor(self.threads)
+        self.desc = (f"{len(rows)} rows of layer 0 ({self.params} params: "
+                     + ", ".join(w.params[i].name.split('.')[-2] for i in rows)
+                     + f"), {len(self.chunks)} chunks on {self.threads} threads")
+
+    def step(self, t):
+        import oracle
+        hp = self.w.hparams
+        if self.w.optimizer == "adamw":
+            f = lambda c: oracle.adamw_step([c[0]], [c[1]], hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], t)
+        elif self.w.optimizer == "sgd":
+            f = lambda c: oracle.sgd_step([c[0]], [c[1]], hp["lr"], hp["momentum"])
+        else:
+            f = lambda c: oracle.lion_step([c[0]], [c[1]], hp["lr"], hp["beta1"], hp["beta2"])
+        list(self.pool.map(f, self.chunks))
+
+    def close(self):
+        self.pool.shutdown()
+
+
+def cpu_baseline(w, rho_bits, seconds):
+    s = OracleSample(w, rho_bits)
+    s.step(1)                                   # warm-up
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        s.step(2 + steps)
+        steps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    s.close()
+    return {"value": s.params * steps / dt, "unit": UNIT, "cores": s.threads, "kind": "oracle",
+            "sample": f"{s.desc}; {steps} steps in {dt:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    from quantized_optimizer_state_gb300 import workloads as wl
+    w = wl.workload(args.workload, args.rho_bits)
+    s = OracleSample(w, args.rho_bits)
+    for t in range(1, args.warmup + 1):
+        s.step(t)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        s.step(args.warmup + 1 + k)
+    dt = time.perf_counter() - t0
+    s.close()
+    value = s.params * args.steps / dt
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": _config(w, args.rho_bits, ws),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": s.threads, "kind": "oracle",
+                         "sample": f"each step: {s.desc}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t_start, t_end):
+        rows = [l for (t, l) in self.lines if t_start - 0.1 <= t <= t_end + 0.3]
+        mhz, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in rows:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def _gpu_id_for_smi(device_index: int) -> str:
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(device_index)
+        return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[device_index] if vis else str(device_index)
+
+
+# ---------------------------------------------------------------------------
+# The GPU arm
+# ---------------------------------------------------------------------------
+
+def _measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _build_states(w, rho_bits, device):
+    import torch
+    from quantized_optimizer_state_gb300 import fo
+    from quantized_optimizer_state_gb300 import workloads as wl
+    states, grads = [], []
+    for i, p in enumerate(w.params):
+        d = fo.CompressedTensor(p.numel, device, rho_bits, w.optimizer == "adamw",
+                                w.hparams["weight_decay"])
+        theta = wl.init_weight_device(p, i, device)
+        d.init_from(theta)
+        del theta
+        states.append(d)
+        grads.append(wl.grad_bf16_device(w.grad, w.grad_scale, p.numel, i, 1, device))
+    torch.cuda.synchronize(device)
+    return states, grads
+
+
+def _stepper(w, table):
+    from quantized_optimizer_state_gb300 import fo
+    hp = w.hparams
+    if w.optimizer == "adamw":
+        return lambda t, s: fo.fo_adamw_step(table, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], t, s)
+    if w.optimizer == "sgd":
+        return lambda t, s: fo.fo_sgd_step(table, hp["lr"], hp["momentum"], s)
+    return lambda t, s: fo.fo_lion_step(table, hp["lr"], hp["beta1"], hp["beta2"], s)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from quantized_optimizer_state_gb300 import fo
+    from quantized_optimizer_state_gb300 import workloads as wl
+
+    ws, rank, local = _dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    def reduce(x, op):
+        if ws == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=op)
+        return float(t.item())
+
+    fo.lib()
+    w = wl.workload(args.workload, args.rho_bits)
+    states, grads = _build_states(w, args.rho_bits, device)
+    table = fo.table_of(states, grads)
+    step = _stepper(w, table)
+    stream = torch.cuda.current_stream(device)
+
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        step(t, stream)
+    torch.cuda.synchronize(device)
+
+    sampler = ClockSampler(_gpu_id_for_smi(local))
+    time.sleep(0.6)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_all0, t_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = fo.fo_kernel_launch_count()
+    barrier()
+    torch.cuda.synchronize(device)
+    wall0 = time.time()
+    t_all0.record(stream)
+    for k in range(args.steps):
+        t += 1
+        ev[k][0].record(stream)
+        step(t, stream)
+        ev[k][1].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    wall1 = time.time()
+    launches = fo.fo_kernel_launch_count() - launches0
+    time.sleep(0.3)
+    sampler.stop()
+    clocks = sampler.summary(wall0, wall1)
+
+    elapsed_ms = t_all0.elapsed_time(t_all1)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    elapsed_ms = reduce(elapsed_ms, dist.ReduceOp.MAX if ws > 1 else None)
+    launches_total = int(reduce(float(launches), dist.ReduceOp.SUM if ws > 1 else None))
+    kernel_ms = statistics.mean(step_ms)     # one library kernel per step on this stream
+    kernel_ms = reduce(kernel_ms, dist.ReduceOp.MAX if ws > 1 else None)
+
+    # end to end through the public API with host buffers: per step, the BF16
+    # gradients go host -> device from pinned memory and the updated BF16
+    # theta' comes back device -> host; the step runs in between.
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(w, states, grads, step, stream, device, args.e2e_steps, t, barrier, reduce, ws)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.rho_bits, args.cpu_seconds)
+
+    if rank == 0:
+        peak, peak_kind = _measured_peak()
+        algo = _algo_bytes(w, args.rho_bits) * w.numel
+        achieved = algo / (kernel_ms * 1e-3) / 1e9
+        out = {
+            "metric": METRIC, "value": ws * w.numel * args.steps / (elapsed_ms * 1e-3), "unit": UNIT,
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": _config(w, args.rho_bits, ws),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "kernel": f"fo_fused_step_kernel<{w.optimizer}>",
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                         else "fallback 6.8 TB/s",
+                         "algorithmic_bytes_per_launch": algo,
+                         "kernel_ms_mean": kernel_ms, "kernel_ms_min": min(step_ms)},
+            "gpu_launches": launches_total,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(out), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _e2e(w, states, grads, step, stream, device, steps, t, barrier, reduce, ws):
+    import torch
+    import torch.distributed as dist
+    biggest = max(p.numel for p in w.params)
+    h_grad = torch.empty(biggest, dtype=torch.bfloat16, pin_memory=True)
+    h_grad.copy_(grads[max(range(len(grads)), key=lambda i: grads[i].numel())].cpu())
+    h_out = torch.empty(biggest, dtype=torch.int16, pin_memory=True)
+    h2d = sum(2 * g.numel() for g in grads)
+    d2h = sum(2 * s.numel for s in states)
+
+    def one(t):
+        for g in grads:
+            g.copy_(h_grad[: g.numel()], non_blocking=True)
+        step(t, stream)
+        for s in states:
+            h_out[: s.numel].copy_(s.theta, non_blocking=True)
+
+    t += 1
+    one(t)                                   # warm-up
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(steps):
+        t += 1
+        one(t)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    ms = e0.elapsed_time(e1)
+    ms = reduce(ms, dist.ReduceOp.MAX if ws > 1 else None)
+    return {"value": ws * w.numel * steps / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps,
+            "path": "pinned host BF16 grads -> device, fo_adamw_step, theta' -> pinned host"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,309 @@
+// fo_api.cu -- the C ABI declared in include/fo.h: argument validation,
+// per-step scalar derivation and kernel launches. No entry point allocates
+// memory, synchronizes, or falls back to the CPU.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include "fo.h"
+#include "fo_internal.h"
+
+namespace fo {
+
+static std::atomic<uint64_t> g_launches{0};
+static thread_local int t_last_cuda_error = 0;
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
+        dev = 0;
+    const int slot = dev & 63;
+    if (cached[slot] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            n = 1;
+        cached[slot] = n;
+    }
+    return cached[slot];
+}
+
+}  // namespace fo
+
+namespace {
+
+using fo::Opt;
+
+fo_status_t cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return FO_OK;
+    fo::t_last_cuda_error = (int)e;
+    return FO_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_finite(double x) { return std::isfinite(x); }
+
+// b^t by repeated squaring in double (the contract in fo.h).
+double pow_by_squaring(double b, int64_t t)
+{
+    double r = 1.0;
+    while (t > 0) {
+        if (t & 1)
+            r *= b;
+        b *= b;
+        t >>= 1;
+    }
+    return r;
+}
+
+bool overlaps(const void *a, int64_t abytes, const void *b, int64_t bbytes)
+{
+    if (!a || !b || abytes <= 0 || bbytes <= 0)
+        return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
+}
+
+fo_status_t check_row(const fo_tensor_t &t, bool with_v)
+{
+    if (t.numel < 0)
+        return FO_ERR_SIZE;
+    if (t.rho_bits != 8 && t.rho_bits != 16)
+        return FO_ERR_BAD_ARG;
+    if (t.reserved != 0 || !is_finite(t.weight_decay))
+        return FO_ERR_BAD_ARG;
+    if (t.numel == 0)
+        return FO_OK;
+    if (t.numel > ((int64_t)1 << 46))
+        return FO_ERR_SIZE;
+    if (!t.theta || !t.rho || !t.m_q || !t.m_scale || !t.grad || (with_v && (!t.v_q || !t.v_scale)))
+        return FO_ERR_NULL;
+    if (!aligned16(t.theta) || !aligned16(t.rho) || !aligned16(t.m_q) || !aligned16(t.grad) ||
+        (with_v && !aligned16(t.v_q)))
+        return FO_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(t.m_scale) & 1u) || (with_v && (reinterpret_cast<uintptr_t>(t.v_scale) & 1u)))
+        return FO_ERR_MISALIGNED;
+    const int64_t n = t.numel, ng = (n + 31) / 32, gb = 2 * n;
+    if (overlaps(t.grad, gb, t.theta, 2 * n) || overlaps(t.grad, gb, t.rho, n * (t.rho_bits / 8)) ||
+        overlaps(t.grad, gb, t.m_q, n) || overlaps(t.grad, gb, t.m_scale, 2 * ng) ||
+        (with_v && (overlaps(t.grad, gb, t.v_q, n) || overlaps(t.grad, gb, t.v_scale, 2 * ng))))
+        return FO_ERR_ALIAS;
+    return FO_OK;
+}
+
+// Per-row scalar: decay (AdamW, Lion) or weight decay (SGD), rounded once to FP32.
+using RowCoef = float (*)(double lr, double weight_decay);
+
+fo_status_t run_table(Opt opt, const fo_tensor_t *table, int32_t ntensors, const fo::StepScalars &s,
+                      double lr, RowCoef coef, fo_stream_t stream)
+{
+    if (ntensors < 0)
+        return FO_ERR_SIZE;
+    if (ntensors > FO_MAX_TENSORS)
+        return FO_ERR_TOO_MANY_TENSORS;
+    if (ntensors == 0)
+        return FO_OK;
+    if (!table)
+        return FO_ERR_NULL;
+    const bool with_v = opt == Opt::kAdamW;
+    for (int32_t i = 0; i < ntensors; ++i) {
+        const fo_status_t st = check_row(table[i], with_v);
+        if (st != FO_OK)
+            return st;
+    }
+
+    // Pack rows into launches of at most kRowsPerLaunch rows and 2^31-1 tiles.
+    static thread_local fo::StepParams p;  // large: kept off the stack
+    p.s = s;
+    int32_t i = 0;
+    while (i < ntensors) {
+        int nrows = 0;
+        int64_t tiles = 0;
+        while (i < ntensors && nrows < fo::kRowsPerLaunch) {
+            const fo_tensor_t &t = table[i];
+            if (t.numel == 0) {
+                ++i;
+                continue;
+            }
+            const int64_t rt = (t.numel + fo::kStepTile - 1) / fo::kStepTile;
+            if (nrows > 0 && tiles + rt > INT32_MAX)
+                break;
+            fo::StepRow &r = p.rows[nrows];
+            r.theta = t.theta;
+            r.rho = t.rho;
+            r.mq = t.m_q;
+            r.ms = t.m_scale;
+            r.vq = with_v ? t.v_q : nullptr;
+            r.vs = with_v ? t.v_scale : nullptr;
+            r.grad = t.grad;
+            r.numel = t.numel;
+            r.coef = coef(lr, t.weight_decay);
+            r.rho_bits = t.rho_bits;
+            tiles += rt;
+            p.tile_end[nrows] = (int32_t)tiles;
+            ++nrows;
+            ++i;
+        }
+        if (nrows == 0)
+            break;
+        p.nrows = nrows;
+        p.total_tiles = (int32_t)tiles;
+        const fo_status_t st = cuda_status(fo::launch_step(opt, p, static_cast<cudaStream_t>(stream)));
+        if (st != FO_OK)
+            return st;
+    }
+    return FO_OK;
+}
+
+float decay_coef(double lr, double wd) { return (float)(1.0 - lr * wd); }
+float wd_coef(double, double wd) { return (float)wd; }
+
+bool beta_ok(double b) { return is_finite(b) && b >= 0.0 && b < 1.0; }
+
+fo_status_t check_codec(const void *a, const void *b, const void *c, int64_t n)
+{
+    if (n < 0)
+        return FO_ERR_SIZE;
+    if (n == 0)
+        return FO_OK;
+    if (!a || !b || !c)
+        return FO_ERR_NULL;
+    return FO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fo_status_t fo_split(const float *theta_f32, uint16_t *theta_bf16, void *rho, int64_t n, int32_t rho_bits,
+                     fo_stream_t stream)
+{
+    fo_status_t st = check_codec(theta_f32, theta_bf16, rho, n);
+    if (st != FO_OK || n == 0)
+        return st;
+    if (rho_bits != 8 && rho_bits != 16)
+        return FO_ERR_BAD_ARG;
+    if (!aligned16(theta_f32) || !aligned16(theta_bf16) || !aligned16(rho))
+        return FO_ERR_MISALIGNED;
+    return cuda_status(fo::launch_split(theta_f32, theta_bf16, rho, n, rho_bits, static_cast<cudaStream_t>(stream)));
+}
+
+fo_status_t fo_merge(const uint16_t *theta_bf16, const void *rho, float *theta_f32, int64_t n, int32_t rho_bits,
+                     fo_stream_t stream)
+{
+    fo_status_t st = check_codec(theta_bf16, rho, theta_f32, n);
+    if (st != FO_OK || n == 0)
+        return st;
+    if (rho_bits != 8 && rho_bits != 16)
+        return FO_ERR_BAD_ARG;
+    if (!aligned16(theta_f32) || !aligned16(theta_bf16) || !aligned16(rho))
+        return FO_ERR_MISALIGNED;
+    return cuda_status(fo::launch_merge(theta_bf16, rho, theta_f32, n, rho_bits, static_cast<cudaStream_t>(stream)));
+}
+
+fo_status_t fo_quant_state(const float *x, void *q, uint16_t *scales, int64_t n, fo_state_kind_t kind,
+                           fo_stream_t stream)
+{
+    fo_status_t st = check_codec(x, q, scales, n);
+    if (st != FO_OK || n == 0)
+        return st;
+    if (kind != FO_STATE_MOMENTUM && kind != FO_STATE_VARIANCE)
+        return FO_ERR_BAD_ARG;
+    if (!aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(scales) & 1u))
+        return FO_ERR_MISALIGNED;
+    return cuda_status(fo::launch_quant(x, q, scales, n, (int)kind, static_cast<cudaStream_t>(stream)));
+}
+
+fo_status_t fo_dequant_state(const void *q, const uint16_t *scales, float *x, int64_t n, fo_state_kind_t kind,
+                             fo_stream_t stream)
+{
+    fo_status_t st = check_codec(q, scales, x, n);
+    if (st != FO_OK || n == 0)
+        return st;
+    if (kind != FO_STATE_MOMENTUM && kind != FO_STATE_VARIANCE)
+        return FO_ERR_BAD_ARG;
+    if (!aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(scales) & 1u))
+        return FO_ERR_MISALIGNED;
+    return cuda_status(fo::launch_dequant(q, scales, x, n, (int)kind, static_cast<cudaStream_t>(stream)));
+}
+
+fo_status_t fo_adamw_step(const fo_tensor_t *table, int32_t ntensors, const fo_adamw_hparams_t *hp, int64_t step,
+                          fo_stream_t stream)
+{
+    if (!hp)
+        return FO_ERR_NULL;
+    if (step < 1)
+        return FO_ERR_SIZE;
+    if (!is_finite(hp->lr) || hp->lr < 0.0 || !beta_ok(hp->beta1) || !beta_ok(hp->beta2) || !is_finite(hp->eps) ||
+        hp->eps <= 0.0)
+        return FO_ERR_BAD_ARG;
+    const double bc1 = 1.0 - pow_by_squaring(hp->beta1, step);
+    const double bc2 = 1.0 - pow_by_squaring(hp->beta2, step);
+    fo::StepScalars s;
+    std::memset(&s, 0, sizeof s);
+    s.a[0] = (float)hp->beta1;
+    s.a[1] = (float)hp->beta2;
+    s.a[2] = (float)(1.0 - hp->beta1);
+    s.a[3] = (float)(1.0 - hp->beta2);
+    s.a[4] = (float)hp->eps;
+    s.a[5] = -(float)(hp->lr / bc1);
+    s.a[6] = (float)(1.0 / std::sqrt(bc2));
+    return run_table(Opt::kAdamW, table, ntensors, s, hp->lr, decay_coef, stream);
+}
+
+fo_status_t fo_sgd_step(const fo_tensor_t *table, int32_t ntensors, const fo_sgd_hparams_t *hp, fo_stream_t stream)
+{
+    if (!hp)
+        return FO_ERR_NULL;
+    if (!is_finite(hp->lr) || hp->lr < 0.0 || !is_finite(hp->momentum) || hp->momentum < 0.0)
+        return FO_ERR_BAD_ARG;
+    fo::StepScalars s;
+    std::memset(&s, 0, sizeof s);
+    s.a[0] = (float)hp->momentum;
+    s.a[1] = -(float)hp->lr;
+    return run_table(Opt::kSgd, table, ntensors, s, hp->lr, wd_coef, stream);
+}
+
+fo_status_t fo_lion_step(const fo_tensor_t *table, int32_t ntensors, const fo_lion_hparams_t *hp,
+                         fo_stream_t stream)
+{
+    if (!hp)
+        return FO_ERR_NULL;
+    if (!is_finite(hp->lr) || hp->lr < 0.0 || !beta_ok(hp->beta1) || !beta_ok(hp->beta2))
+        return FO_ERR_BAD_ARG;
+    fo::StepScalars s;
+    std::memset(&s, 0, sizeof s);
+    s.a[0] = (float)hp->beta1;
+    s.a[1] = (float)hp->beta2;
+    s.a[2] = (float)(1.0 - hp->beta1);
+    s.a[3] = (float)(1.0 - hp->beta2);
+    s.a[4] = -(float)hp->lr;
+    return run_table(Opt::kLion, table, ntensors, s, hp->lr, decay_coef, stream);
+}
+
+const char *fo_status_string(fo_status_t status)
+{
+    switch (status) {
+    case FO_OK: return "FO_OK";
+    case FO_ERR_NULL: return "FO_ERR_NULL: a required pointer is NULL";
+    case FO_ERR_MISALIGNED: return "FO_ERR_MISALIGNED: an element array is not 16-byte aligned";
+    case FO_ERR_SIZE: return "FO_ERR_SIZE: a count is negative or too large";
+    case FO_ERR_BAD_ARG: return "FO_ERR_BAD_ARG: a flag or hyper-parameter is out of range";
+    case FO_ERR_TOO_MANY_TENSORS: return "FO_ERR_TOO_MANY_TENSORS: ntensors exceeds FO_MAX_TENSORS";
+    case FO_ERR_CUDA: return "FO_ERR_CUDA: a CUDA call failed";
+    case FO_ERR_ALIAS: return "FO_ERR_ALIAS: grad overlaps a state buffer";
+    }
+    return "unknown fo_status_t";
+}
+
+int fo_last_cuda_error(void) { return fo::t_last_cuda_error; }
+
+uint64_t fo_kernel_launch_count(void) { return fo::g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// fo_internal.h -- interface between the C-ABI layer (fo_api.cu) and the
+// kernels (fo_step.cu, fo_codecs.cu). Not installed; not part of the ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fo {
+
+constexpr int kGroup = 32;           // quantization group (page: G = 32)
+constexpr int kElemsPerThread = 16;  // one thread holds half a group
+constexpr int kStepThreads = 256;
+constexpr int kStepTile = kStepThreads * kElemsPerThread;  // 4096 elements per tile
+
+enum class Opt : int { kAdamW = 0, kSgd = 1, kLion = 2 };
+
+// One table row as the step kernel sees it. `coef` is the per-tensor scalar:
+// the decay factor (1 - lr*wd) for AdamW and Lion, the weight decay for SGD.
+struct StepRow {
+    uint16_t *theta;
+    void *rho;
+    int8_t *mq;
+    uint16_t *ms;
+    uint8_t *vq;
+    uint16_t *vs;
+    const uint16_t *grad;
+    int64_t numel;
+    float coef;
+    int32_t rho_bits;
+};
+static_assert(sizeof(StepRow) == 72, "StepRow layout");
+
+// Per-step FP32 scalars.
+//  AdamW: a = {beta1, beta2, 1-beta1, 1-beta2, eps, -lr/bc1, 1/sqrt(bc2)}
+//  SGD:   a = {momentum, -lr}
+//  Lion:  a = {beta1, beta2, 1-beta1, 1-beta2, -lr}
+struct StepScalars {
+    float a[8];
+};
+
+// Rows per launch: the whole table of one launch travels in the kernel's
+// parameter space (at most 32764 bytes on sm_70 and later).
+constexpr int kRowsPerLaunch = 384;
+
+struct StepParams {
+    StepScalars s;
+    int32_t nrows;
+    int32_t total_tiles;
+    int32_t tile_end[kRowsPerLaunch];  // inclusive prefix sums of tiles per row
+    StepRow rows[kRowsPerLaunch];
+};
+static_assert(sizeof(StepParams) <= 32764, "kernel parameter space");
+
+// Launch one fused step over p.nrows rows (p.total_tiles > 0).
+cudaError_t launch_step(Opt opt, const StepParams &p, cudaStream_t stream);
+
+// Element-wise codecs.
+cudaError_t launch_split(const float *theta, uint16_t *tp, void *rho, int64_t n, int rho_bits,
+                         cudaStream_t stream);
+cudaError_t launch_merge(const uint16_t *tp, const void *rho, float *theta, int64_t n, int rho_bits,
+                         cudaStream_t stream);
+cudaError_t launch_quant(const float *x, void *q, uint16_t *scales, int64_t n, int kind,
+                         cudaStream_t stream);
+cudaError_t launch_dequant(const void *q, const uint16_t *scales, float *x, int64_t n, int kind,
+                           cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+// Kernel launches issued by this library so far.
+void count_launch();
+
+}  // namespace fo

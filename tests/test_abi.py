@@ -1,0 +1,119 @@
+"""The C-ABI library builds, loads and exports what include/fo.h declares.
+
+No compute call is made here: every call below is rejected by the host-side
+argument checks before anything touches CUDA, so these run without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from quantized_optimizer_state_gb300 import fo
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "fo.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fo_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    lib = fo.lib()
+    names = _declared_functions()
+    assert "fo_adamw_step" in names and "fo_split" in names and len(names) >= 10
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(fo.SIGNATURES)
+
+
+def test_struct_layout_matches_header():
+    # 7 pointers, int64 numel, double weight_decay, int32 rho_bits, int32 reserved
+    assert ctypes.sizeof(fo.FoTensor) == 80
+    assert fo.FoTensor.numel.offset == 56 and fo.FoTensor.weight_decay.offset == 64
+    assert ctypes.sizeof(fo.AdamWHparams) == 32
+
+
+def test_status_strings():
+    for code, name in fo.STATUS.items():
+        assert fo.fo_status_string(code).startswith(name)
+    assert "unknown" in fo.fo_status_string(99)
+
+
+def _call(fn, *args):
+    return getattr(fo.lib(), fn)(*args)
+
+
+def test_codec_argument_errors():
+    A = 1 << 20          # a 16-byte aligned fake address: never dereferenced
+    assert _call("fo_split", A, A, A, 0, 8, None) == 0                  # n = 0 is a no-op
+    assert _call("fo_split", A, A, A, -1, 8, None) == 3                 # FO_ERR_SIZE
+    assert _call("fo_split", None, A, A, 10, 8, None) == 1              # FO_ERR_NULL
+    assert _call("fo_split", A, A, A, 10, 12, None) == 4                # rho_bits
+    assert _call("fo_split", A + 2, A, A, 10, 8, None) == 2             # misaligned
+    assert _call("fo_merge", A, A + 8, A, 10, 16, None) == 2
+    assert _call("fo_quant_state", A, A, A, 10, 7, None) == 4           # bad kind
+    assert _call("fo_quant_state", A, A, A + 1, 10, 0, None) == 2       # odd scale address
+    assert _call("fo_dequant_state", A, None, A, 10, 1, None) == 1
+
+
+def _table(**over):
+    A = 1 << 24
+    base = dict(theta=A, rho=A + (1 << 20), m_q=A + (2 << 20), m_scale=A + (3 << 20),
+                v_q=A + (4 << 20), v_scale=A + (5 << 20), grad=A + (6 << 20), numel=100,
+                weight_decay=0.01, rho_bits=8, reserved=0)
+    base.update(over)
+    return fo.FoTensor(**base)
+
+
+def _adamw(rows, step=1, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8):
+    arr = (fo.FoTensor * max(1, len(rows)))(*rows)
+    hp = fo.AdamWHparams(lr, beta1, beta2, eps)
+    return _call("fo_adamw_step", ctypes.addressof(arr), len(rows), ctypes.addressof(hp), step, None)
+
+
+def test_step_argument_errors():
+    assert _adamw([]) == 0                                         # empty table: no-op
+    assert _adamw([_table(numel=0)]) == 0                          # empty rows are skipped
+    assert _adamw([_table()], step=0) == 3
+    assert _adamw([_table(numel=-5)]) == 3
+    assert _adamw([_table(theta=None)]) == 1
+    assert _adamw([_table(v_q=None)]) == 1                         # AdamW needs v
+    assert _adamw([_table(rho_bits=4)]) == 4
+    assert _adamw([_table(reserved=1)]) == 4
+    assert _adamw([_table(weight_decay=float("nan"))]) == 4
+    assert _adamw([_table(grad=(1 << 24) + (6 << 20) + 8)]) == 2   # misaligned grad
+    assert _adamw([_table(m_scale=(1 << 24) + (3 << 20) + 1)]) == 2
+    assert _adamw([_table(grad=(1 << 24) + 64)]) == 7              # grad overlaps theta'
+    assert _adamw([_table()], lr=float("inf")) == 4
+    assert _adamw([_table()], beta1=1.0) == 4
+    assert _adamw([_table()], eps=0.0) == 4
+    assert _adamw([_table(), _table(numel=-1)]) == 3               # checked before any launch
+    hp = fo.AdamWHparams(1e-3, 0.9, 0.999, 1e-8)
+    assert _call("fo_adamw_step", None, 3, ctypes.addressof(hp), 1, None) == 1
+    assert _call("fo_adamw_step", None, -1, ctypes.addressof(hp), 1, None) == 3
+    assert _call("fo_adamw_step", None, fo.FO_MAX_TENSORS + 1, ctypes.addressof(hp), 1, None) == 5
+    arr = (fo.FoTensor * 1)(_table())
+    assert _call("fo_adamw_step", ctypes.addressof(arr), 1, None, 1, None) == 1
+
+
+def test_sgd_and_lion_need_no_v():
+    arr = (fo.FoTensor * 1)(_table(v_q=None, v_scale=None, numel=-1))
+    sgd = fo.SGDHparams(0.1, 0.9)
+    lion = fo.LionHparams(1e-4, 0.9, 0.99)
+    # the v pointers are not required; the bad numel is what is reported
+    assert _call("fo_sgd_step", ctypes.addressof(arr), 1, ctypes.addressof(sgd), None) == 3
+    assert _call("fo_lion_step", ctypes.addressof(arr), 1, ctypes.addressof(lion), None) == 3
+    bad = fo.SGDHparams(-0.1, 0.9)
+    assert _call("fo_sgd_step", ctypes.addressof(arr), 1, ctypes.addressof(bad), None) == 4
+    badl = fo.LionHparams(1e-4, 0.9, 1.5)
+    assert _call("fo_lion_step", ctypes.addressof(arr), 1, ctypes.addressof(badl), None) == 4
+
+
+def test_rejected_calls_launch_nothing():
+    before = fo.fo_kernel_launch_count()
+    assert _adamw([_table(rho_bits=3)]) == 4
+    assert _call("fo_split", 16, 16, 16, -1, 8, None) == 3
+    assert fo.fo_kernel_launch_count() == before
