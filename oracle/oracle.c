@@ -169,9 +169,11 @@ static uint16_t bf16_adjacent(uint16_t b, int dir)
  */
 float oracle_half_ulp(uint16_t theta_p, int dir)
 {
-    float a = oracle_bf16_to_f32(theta_p);
-    float b = oracle_bf16_to_f32(bf16_adjacent(theta_p, dir));
-    return fabsf(b - a) * 0.5f; /* neighbours: the difference and the halving are exact */
+    /* Past the largest finite BF16 the next value is taken as 2^128, as IEEE
+     * rounding treats overflow (unbounded exponent), so the gap stays 2^120. */
+    double a = bf16_value_unbounded(theta_p);
+    double b = bf16_value_unbounded(bf16_adjacent(theta_p, dir));
+    return (float)(fabs(b - a) * 0.5); /* neighbours: exact in double, and a power of two */
 }
 
 /* ------------------------------------------------------------------------ */

@@ -94,8 +94,8 @@ def test_half_ulp_all_finite_bf16(orc):
     up = orc.half_ulp_n(arr, +1).astype(np.float64)
     dn = orc.half_ulp_n(arr, -1).astype(np.float64)
     for i, b in enumerate(pats):
-        if (b & 0x7FFF) == 0x7F7F:
-            continue                                             # neighbour is infinite
+        # past the largest finite BF16 the gap is that of its binade (IEEE's
+        # unbounded-exponent rounding), 2^(127-7)
         assert up[i] == _gap_closed_form(b, +1) / 2, hex(b)
         assert dn[i] == _gap_closed_form(b, -1) / 2, hex(b)
 
@@ -109,3 +109,6 @@ def test_half_ulp_bound_examples(orc):
     assert orc.half_ulp(0x8000, -1) == 2.0 ** -134
     # smallest normal 2^-126: the subnormals below are spaced like the binade above
     assert orc.half_ulp(0x0080, -1) == 2.0 ** -134
+    # largest finite BF16: the gap above is its binade's, not infinite
+    assert orc.half_ulp(0x7F7F, +1) == 2.0 ** 119
+    assert orc.half_ulp(0xFF7F, -1) == 2.0 ** 119
