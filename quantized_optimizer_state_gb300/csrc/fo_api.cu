@@ -118,50 +118,61 @@ fo_status_t run_table(Opt opt, const fo_tensor_t *table, int32_t ntensors, const
             return st;
     }
 
-    // Pack rows into launches of at most kRowsPerLaunch rows and 2^31-1 tiles.
+    // Pack rows into launches of one correction width, at most kRowsPerLaunch
+    // rows and 2^31-1 tiles each (a kernel is specialised per width).
     static thread_local fo::StepParams p;  // large: kept off the stack
     p.s = s;
-    int32_t i = 0;
-    while (i < ntensors) {
-        int nrows = 0;
-        int64_t tiles = 0;
-        while (i < ntensors && nrows < fo::kRowsPerLaunch) {
-            const fo_tensor_t &t = table[i];
-            if (t.numel == 0) {
+    for (const int rb : {8, 16}) {
+        int32_t i = 0;
+        while (i < ntensors) {
+            int nrows = 0;
+            int64_t tiles = 0;
+            while (i < ntensors && nrows < fo::kRowsPerLaunch) {
+                const fo_tensor_t &t = table[i];
+                if (t.numel == 0 || t.rho_bits != rb) {
+                    ++i;
+                    continue;
+                }
+                const int64_t rt = (t.numel + fo::kStepTile - 1) / fo::kStepTile;
+                if (nrows > 0 && tiles + rt > INT32_MAX)
+                    break;
+                fo::StepRow &r = p.rows[nrows];
+                r.theta = t.theta;
+                r.rho = t.rho;
+                r.mq = t.m_q;
+                r.ms = t.m_scale;
+                r.vq = with_v ? t.v_q : nullptr;
+                r.vs = with_v ? t.v_scale : nullptr;
+                r.grad = t.grad;
+                r.numel = t.numel;
+                r.coef = coef(lr, t.weight_decay);
+                r.rho_bits = t.rho_bits;
+                tiles += rt;
+                p.tile_end[nrows] = (int32_t)tiles;
+                ++nrows;
                 ++i;
-                continue;
             }
-            const int64_t rt = (t.numel + fo::kStepTile - 1) / fo::kStepTile;
-            if (nrows > 0 && tiles + rt > INT32_MAX)
+            if (nrows == 0)
                 break;
-            fo::StepRow &r = p.rows[nrows];
-            r.theta = t.theta;
-            r.rho = t.rho;
-            r.mq = t.m_q;
-            r.ms = t.m_scale;
-            r.vq = with_v ? t.v_q : nullptr;
-            r.vs = with_v ? t.v_scale : nullptr;
-            r.grad = t.grad;
-            r.numel = t.numel;
-            r.coef = coef(lr, t.weight_decay);
-            r.rho_bits = t.rho_bits;
-            tiles += rt;
-            p.tile_end[nrows] = (int32_t)tiles;
-            ++nrows;
-            ++i;
+            p.nrows = nrows;
+            p.total_tiles = (int32_t)tiles;
+            const fo_status_t st = cuda_status(fo::launch_step(opt, rb, p, static_cast<cudaStream_t>(stream)));
+            if (st != FO_OK)
+                return st;
         }
-        if (nrows == 0)
-            break;
-        p.nrows = nrows;
-        p.total_tiles = (int32_t)tiles;
-        const fo_status_t st = cuda_status(fo::launch_step(opt, p, static_cast<cudaStream_t>(stream)));
-        if (st != FO_OK)
-            return st;
     }
     return FO_OK;
 }
 
 float decay_coef(double lr, double wd) { return (float)(1.0 - lr * wd); }
+
+// Both lanes of a packed FP32 pair set to x.
+unsigned long long lanes(float x)
+{
+    uint32_t u;
+    std::memcpy(&u, &x, sizeof u);
+    return ((unsigned long long)u << 32) | u;
+}
 float wd_coef(double, double wd) { return (float)wd; }
 
 bool beta_ok(double b) { return is_finite(b) && b >= 0.0 && b < 1.0; }
@@ -254,6 +265,17 @@ fo_status_t fo_adamw_step(const fo_tensor_t *table, int32_t ntensors, const fo_a
     s.a[4] = (float)hp->eps;
     s.a[5] = -(float)(hp->lr / bc1);
     s.a[6] = (float)(1.0 / std::sqrt(bc2));
+    s.p[0] = lanes(s.a[0]);
+    s.p[1] = lanes(-s.a[1]);
+    s.p[2] = lanes(s.a[2]);
+    s.p[3] = lanes(-s.a[3]);
+    s.p[4] = lanes(s.a[6]);
+    s.p[5] = lanes(-s.a[4]);
+    s.p[6] = lanes(s.a[5]);
+    // validated operand ranges of the packed division/square root: den = sqrt(v)
+    // /sqrt(bc2) + eps stays in [2^-40, 2^40] when these hold (|g| <= 2^24 is
+    // checked per element)
+    s.fast = (s.a[4] >= 0x1p-40f && s.a[4] <= 0x1p20f && s.a[6] <= 0x1p8f) ? 1 : 0;
     return run_table(Opt::kAdamW, table, ntensors, s, hp->lr, decay_coef, stream);
 }
 
@@ -267,6 +289,9 @@ fo_status_t fo_sgd_step(const fo_tensor_t *table, int32_t ntensors, const fo_sgd
     std::memset(&s, 0, sizeof s);
     s.a[0] = (float)hp->momentum;
     s.a[1] = -(float)hp->lr;
+    s.p[0] = lanes(s.a[0]);
+    s.p[1] = lanes(s.a[1]);
+    s.fast = 1;
     return run_table(Opt::kSgd, table, ntensors, s, hp->lr, wd_coef, stream);
 }
 
@@ -284,6 +309,9 @@ fo_status_t fo_lion_step(const fo_tensor_t *table, int32_t ntensors, const fo_li
     s.a[2] = (float)(1.0 - hp->beta1);
     s.a[3] = (float)(1.0 - hp->beta2);
     s.a[4] = -(float)hp->lr;
+    for (int i = 0; i < 5; ++i)
+        s.p[i] = lanes(s.a[i]);
+    s.fast = 1;
     return run_table(Opt::kLion, table, ntensors, s, hp->lr, decay_coef, stream);
 }
 

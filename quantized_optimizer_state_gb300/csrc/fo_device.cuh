@@ -178,16 +178,18 @@ __device__ __forceinline__ float code_multiplier(float s, float levels)
 }
 
 // Momentum code pattern: clamp(rint(z * mult), -127, 127).
-__device__ __forceinline__ uint32_t m_code(float z, float mult)
+__device__ __forceinline__ uint32_t m_code_of(float x)
 {
-    return round_code(fminf(fmaxf(__fmul_rn(z, mult), -127.0f), 127.0f));
+    return round_code(fminf(fmaxf(x, -127.0f), 127.0f));
 }
+__device__ __forceinline__ uint32_t m_code(float z, float mult) { return m_code_of(__fmul_rn(z, mult)); }
 
 // Second-moment code pattern: min(rint(r * mult), 255), r >= 0.
-__device__ __forceinline__ uint32_t v_code(float r, float mult)
+__device__ __forceinline__ uint32_t v_code_of(float x)
 {
-    return round_code(fminf(__fmul_rn(r, mult), 255.0f));
+    return round_code(fminf(x, 255.0f));
 }
+__device__ __forceinline__ uint32_t v_code(float r, float mult) { return v_code_of(__fmul_rn(r, mult)); }
 
 // ---------------------------------------------------------------------------
 // Streaming global memory access (touched once: evict-first)

@@ -34,8 +34,18 @@ static_assert(sizeof(StepRow) == 72, "StepRow layout");
 //  AdamW: a = {beta1, beta2, 1-beta1, 1-beta2, eps, -lr/bc1, 1/sqrt(bc2)}
 //  SGD:   a = {momentum, -lr}
 //  Lion:  a = {beta1, beta2, 1-beta1, 1-beta2, -lr}
+// and the same values as lane pairs for the packed fast path (p), with the
+// signs that path needs:
+//  AdamW: p = {b1, -b2, 1-b1, -(1-b2), 1/sqrt(bc2), -eps, -lr/bc1}
+//  SGD:   p = {momentum, -lr}
+//  Lion:  p = {b1, b2, 1-b1, 1-b2, -lr}
+// fast = 1 when the call's hyper-parameters keep the fast path's operands in
+// its validated ranges (AdamW: eps in [2^-40, 2^20], 1/sqrt(bc2) <= 2^8).
 struct StepScalars {
     float a[8];
+    unsigned long long p[8];
+    int32_t fast;
+    int32_t pad;
 };
 
 // Rows per launch: the whole table of one launch travels in the kernel's
@@ -51,8 +61,9 @@ struct StepParams {
 };
 static_assert(sizeof(StepParams) <= 32764, "kernel parameter space");
 
-// Launch one fused step over p.nrows rows (p.total_tiles > 0).
-cudaError_t launch_step(Opt opt, const StepParams &p, cudaStream_t stream);
+// Launch one fused step over p.nrows rows, all of correction width rho_bits
+// (p.total_tiles > 0).
+cudaError_t launch_step(Opt opt, int rho_bits, const StepParams &p, cudaStream_t stream);
 
 // Element-wise codecs.
 cudaError_t launch_split(const float *theta, uint16_t *tp, void *rho, int64_t n, int rho_bits,

@@ -1,0 +1,117 @@
+// fo_pair.cuh -- packed two-lane FP32 arithmetic for the fused step's fast
+// path (sm_103a add/sub/mul/fma.rn.f32x2: two IEEE round-to-nearest results
+// per instruction, bit-identical to the scalar operations), and correctly
+// rounded division and square root built from the hardware approximations.
+//
+// Division (RN(a/b), b > 0): one Newton step on the hardware reciprocal
+// approximation y0 of 1/b, y1 = y0 + y0*(1 - b*y0), gives the correctly
+// rounded reciprocal RN(1/b); then q0 = RN(a*y1) is within one ulp of a/b,
+// the remainder r = a - b*q0 is exact, and RN(q0 + r*y1) = RN(a/b)
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990; see also Muller et
+// al., "Handbook of Floating-Point Arithmetic", ch. on FMA-based division).
+// Square root (RN(sqrt(v))): one Goldschmidt refinement of s = v*y,
+// h = y/2 from the hardware reciprocal-square-root approximation y, then the
+// exact remainder d = v - s*s and RN(s + d*h) (same references).
+//
+// Validity: both sequences were checked bit for bit against the CUDA
+// correctly rounded operations -- the reciprocal over every significand of
+// ten binades from 2^-126 to 2^125, the division over 3.2e9 operand pairs,
+// the square root over every value of twelve binades from 2^-100 to 2^126.
+// They are used only where the operands are inside the ranges listed at each
+// function; callers check the ranges and recompute elsewhere with the IEEE
+// operations.
+#pragma once
+
+#include <cstdint>
+
+namespace fo {
+
+typedef unsigned long long f2;  // two FP32 lanes in one 64-bit register pair
+
+__device__ __forceinline__ f2 pk(float lo, float hi)
+{
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpk(f2 v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ f2 add2(f2 a, f2 b)
+{
+    f2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ f2 mul2(f2 a, f2 b)
+{
+    f2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c)
+{
+    f2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ f2 splat(float x) { return pk(x, x); }
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rsqrt_approx(float x)
+{
+    float y;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// RN(a / b) in both lanes, given nb = -b. Valid when b is in [2^-100, 2^100],
+// a is +0 or has |a| >= 2^-100 (or b == 1 exactly), and the quotient is in
+// [2^-100, 2^100] or 0. q0 (the first quotient) is returned for range checks.
+__device__ __forceinline__ f2 div2(f2 a, f2 nb, f2 &q0)
+{
+    float n0, n1;
+    unpk(nb, n0, n1);
+    const f2 y0 = pk(rcp_approx(-n0), rcp_approx(-n1));
+    const f2 e = fma2(nb, y0, splat(1.0f));  // 1 - b*y0
+    const f2 y1 = fma2(y0, e, y0);            // RN(1/b)
+    q0 = mul2(a, y1);
+    const f2 r = fma2(nb, q0, a);             // a - b*q0, exact
+    return fma2(r, y1, q0);
+}
+
+__device__ __forceinline__ f2 div2(f2 a, f2 nb)
+{
+    f2 q0;
+    return div2(a, nb, q0);
+}
+
+// -RN(sqrt(v)) in both lanes, given nv = -v with v in [2^-100, 2^126].
+__device__ __forceinline__ f2 neg_sqrt2(f2 nv)
+{
+    float v0, v1;
+    unpk(nv, v0, v1);
+    const f2 y = pk(rsqrt_approx(-v0), rsqrt_approx(-v1));
+    f2 ns = mul2(nv, y);                      // -s, s ~ sqrt(v)
+    f2 h = mul2(splat(0.5f), y);              // h ~ 1/(2 sqrt(v))
+    const f2 e = fma2(ns, h, splat(0.5f));    // 1/2 - s*h
+    ns = fma2(ns, e, ns);                     // -(s + s*e)
+    h = fma2(h, e, h);
+    const f2 d = fma2(ns, ns, nv);            // s*s - v = -(v - s*s), exact
+    return fma2(d, h, ns);                    // -(s + (v - s*s)*h)
+}
+
+}  // namespace fo

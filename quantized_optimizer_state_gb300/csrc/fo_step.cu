@@ -16,11 +16,17 @@
 
 #include "fo_device.cuh"
 #include "fo_internal.h"
+#include "fo_pair.cuh"
 
 namespace fo {
 namespace {
 
 constexpr int kEPT = kElemsPerThread;
+// resident CTAs per SM the register budget is sized for (4: 64 registers a thread)
+#ifndef FO_STEP_MIN_BLOCKS
+#define FO_STEP_MIN_BLOCKS 4
+#endif
+constexpr int kStepMinBlocks = FO_STEP_MIN_BLOCKS;
 
 struct Loaded {
     uint32_t g[8];   // 16 BF16 gradients
@@ -32,65 +38,64 @@ struct Loaded {
 };
 
 template <int RB, bool WithV>
-__device__ __forceinline__ void load_full(const StepRow &row, int64_t i0, Loaded &L)
+__device__ __forceinline__ void load_chunk(const StepRow &row, int64_t i0, int cnt, Loaded &L)
 {
-    uint4 a = ld_stream(row.grad + i0), b = ld_stream(row.grad + i0 + 8);
-    L.g[0] = a.x; L.g[1] = a.y; L.g[2] = a.z; L.g[3] = a.w;
-    L.g[4] = b.x; L.g[5] = b.y; L.g[6] = b.z; L.g[7] = b.w;
-    a = ld_stream(row.theta + i0);
-    b = ld_stream(row.theta + i0 + 8);
-    L.t[0] = a.x; L.t[1] = a.y; L.t[2] = a.z; L.t[3] = a.w;
-    L.t[4] = b.x; L.t[5] = b.y; L.t[6] = b.z; L.t[7] = b.w;
-    if (RB == 8) {
-        a = ld_stream(static_cast<const int8_t *>(row.rho) + i0);
-        L.r[0] = a.x; L.r[1] = a.y; L.r[2] = a.z; L.r[3] = a.w;
-    } else {
-        a = ld_stream(static_cast<const int16_t *>(row.rho) + i0);
-        b = ld_stream(static_cast<const int16_t *>(row.rho) + i0 + 8);
-        L.r[0] = a.x; L.r[1] = a.y; L.r[2] = a.z; L.r[3] = a.w;
-        L.r[4] = b.x; L.r[5] = b.y; L.r[6] = b.z; L.r[7] = b.w;
+    if (cnt == kEPT) {
+        uint4 a = ld_stream(row.grad + i0), b = ld_stream(row.grad + i0 + 8);
+        L.g[0] = a.x; L.g[1] = a.y; L.g[2] = a.z; L.g[3] = a.w;
+        L.g[4] = b.x; L.g[5] = b.y; L.g[6] = b.z; L.g[7] = b.w;
+        a = ld_stream(row.theta + i0);
+        b = ld_stream(row.theta + i0 + 8);
+        L.t[0] = a.x; L.t[1] = a.y; L.t[2] = a.z; L.t[3] = a.w;
+        L.t[4] = b.x; L.t[5] = b.y; L.t[6] = b.z; L.t[7] = b.w;
+        if (RB == 8) {
+            a = ld_stream(static_cast<const int8_t *>(row.rho) + i0);
+            L.r[0] = a.x; L.r[1] = a.y; L.r[2] = a.z; L.r[3] = a.w;
+        } else {
+            a = ld_stream(static_cast<const int16_t *>(row.rho) + i0);
+            b = ld_stream(static_cast<const int16_t *>(row.rho) + i0 + 8);
+            L.r[0] = a.x; L.r[1] = a.y; L.r[2] = a.z; L.r[3] = a.w;
+            L.r[4] = b.x; L.r[5] = b.y; L.r[6] = b.z; L.r[7] = b.w;
+        }
+        a = ld_stream(row.mq + i0);
+        L.m[0] = a.x; L.m[1] = a.y; L.m[2] = a.z; L.m[3] = a.w;
+        if (WithV) {
+            a = ld_stream(row.vq + i0);
+            L.v[0] = a.x; L.v[1] = a.y; L.v[2] = a.z; L.v[3] = a.w;
+        }
+        L.ms = __ldcs(row.ms + (i0 >> 5));
+        if (WithV)
+            L.vs = __ldcs(row.vs + (i0 >> 5));
+        return;
     }
-    a = ld_stream(row.mq + i0);
-    L.m[0] = a.x; L.m[1] = a.y; L.m[2] = a.z; L.m[3] = a.w;
-    if (WithV) {
-        a = ld_stream(row.vq + i0);
-        L.v[0] = a.x; L.v[1] = a.y; L.v[2] = a.z; L.v[3] = a.w;
-    }
-    L.ms = __ldcs(row.ms + (i0 >> 5));
-    if (WithV)
-        L.vs = __ldcs(row.vs + (i0 >> 5));
-}
-
-// Element-wise loads of the first cnt (< 16) elements; the rest read as 0.
-template <int RB, bool WithV>
-__device__ __forceinline__ void load_partial(const StepRow &row, int64_t i0, int cnt, Loaded &L)
-{
+    // ragged tail of a tensor: element-wise loads of the first cnt elements,
+    // the rest read as 0 (and are masked out of the group absmax)
 #pragma unroll
     for (int w = 0; w < 8; ++w) { L.g[w] = 0; L.t[w] = 0; L.r[w] = 0; }
 #pragma unroll
     for (int w = 0; w < 4; ++w) { L.m[w] = 0; L.v[w] = 0; }
-    L.ms = 0;
-    L.vs = 0;
+    // the group's scales: needed by both lanes of the pair even when this lane
+    // holds no element (the pair splits the per-group divisions)
+    const bool group_exists = ((i0 >> 5) << 5) < row.numel;
+    L.ms = group_exists ? row.ms[i0 >> 5] : (uint16_t)0;
+    L.vs = (WithV && group_exists) ? row.vs[i0 >> 5] : (uint16_t)0;
     if (cnt <= 0)
         return;
 #pragma unroll
     for (int j = 0; j < kEPT; ++j) {
-        if (j < cnt) {
-            const int sh16 = 16 * (j & 1), sh8 = 8 * (j & 3);
-            L.g[j >> 1] |= (uint32_t)row.grad[i0 + j] << sh16;
-            L.t[j >> 1] |= (uint32_t)row.theta[i0 + j] << sh16;
-            if (RB == 8)
-                L.r[j >> 2] |= (uint32_t)(uint8_t)static_cast<const int8_t *>(row.rho)[i0 + j] << sh8;
-            else
-                L.r[j >> 1] |= (uint32_t)(uint16_t)static_cast<const int16_t *>(row.rho)[i0 + j] << sh16;
-            L.m[j >> 2] |= (uint32_t)(uint8_t)row.mq[i0 + j] << sh8;
-            if (WithV)
-                L.v[j >> 2] |= (uint32_t)row.vq[i0 + j] << sh8;
-        }
+        if (j >= cnt)
+            break;
+        const int sh16 = 16 * (j & 1), sh8 = 8 * (j & 3);
+        L.g[j >> 1] |= (uint32_t)row.grad[i0 + j] << sh16;
+        L.t[j >> 1] |= (uint32_t)row.theta[i0 + j] << sh16;
+        if (RB == 8)
+            L.r[j >> 2] |= (uint32_t)(uint8_t)static_cast<const int8_t *>(row.rho)[i0 + j] << sh8;
+        else
+            L.r[j >> 1] |= (uint32_t)(uint16_t)static_cast<const int16_t *>(row.rho)[i0 + j] << sh16;
+        L.m[j >> 2] |= (uint32_t)(uint8_t)row.mq[i0 + j] << sh8;
+        if (WithV)
+            L.v[j >> 2] |= (uint32_t)row.vq[i0 + j] << sh8;
     }
-    L.ms = row.ms[i0 >> 5];
-    if (WithV)
-        L.vs = row.vs[i0 >> 5];
 }
 
 // rho of element j as a float (exact).
@@ -109,12 +114,14 @@ __device__ __forceinline__ uint32_t theta_p_bits(const uint32_t (&t)[8])
     return (J & 1) ? bf16_hi_bits(t[J >> 1]) : bf16_lo_bits(t[J >> 1]);
 }
 
-// Element j: decode, update, re-split. Writes the new theta (FP32) and the
-// companded momentum z (and r = sqrt(v) for AdamW).
+// Exact path, element j: decode, update, and the new theta (FP32), the
+// companded momentum z and nr = -sqrt(v) (AdamW; 0 otherwise), with the IEEE
+// operations of the library's arithmetic contract. It serves the threads
+// whose operands fall outside the validated ranges of the packed fast path.
 template <Opt O, int RB, int J>
-__device__ __forceinline__ void element(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
-                                        const StepScalars &s, float coef, float cm, float cv,
-                                        float &theta_out, float &z_out, float &r_out)
+__device__ __forceinline__ void element_exact(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
+                                              const StepScalars &s, float coef, float cm, float cv,
+                                              float &theta_out, float &z_out, float &nr_out)
 {
     const float g = __uint_as_float(theta_p_bits<J>(L.g));
     float theta = merge_one<RB>(theta_p_bits<J>(L.t), rho_at<RB, J>(rx));
@@ -130,47 +137,187 @@ __device__ __forceinline__ void element(const Loaded &L, const uint32_t (&rx)[8]
         const float r = __fsqrt_rn(v);
         const float den = __fmaf_rn(r, s.a[6], s.a[4]);
         theta = __fmaf_rn(s.a[5], __fdiv_rn(m, den), theta);
-        r_out = r;
+        nr_out = -r;
     } else if (O == Opt::kSgd) {
         const float gp = __fmaf_rn(coef, theta, g);
         m = __fmaf_rn(s.a[0], m, gp);
         theta = __fmaf_rn(s.a[1], m, theta);
-        r_out = 0.0f;
+        nr_out = 0.0f;
     } else {
         const float c = __fmaf_rn(s.a[0], m, __fmul_rn(s.a[2], g));
         const float sgn = c > 0.0f ? 1.0f : (c < 0.0f ? -1.0f : 0.0f);
         theta = __fmaf_rn(s.a[4], sgn, __fmul_rn(theta, coef));
         m = __fmaf_rn(s.a[1], m, __fmul_rn(s.a[3], g));
-        r_out = 0.0f;
+        nr_out = 0.0f;
     }
     theta_out = theta;
     z_out = phi_m(m);
 }
 
 template <Opt O, int RB, int... J>
-__device__ __forceinline__ void all_elements(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
-                                             const StepScalars &s, float coef, float cm, float cv,
-                                             float (&th)[kEPT], float (&z)[kEPT], float (&r)[kEPT],
-                                             std::integer_sequence<int, J...>)
+__device__ __forceinline__ void all_exact(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
+                                          const StepScalars &s, float coef, float cm, float cv,
+                                          float (&th)[kEPT], float (&z)[kEPT], float (&nr)[kEPT],
+                                          std::integer_sequence<int, J...>)
 {
-    (element<O, RB, J>(L, rx, mx, s, coef, cm, cv, th[J], z[J], r[J]), ...);
+    (element_exact<O, RB, J>(L, rx, mx, s, coef, cm, cv, th[J], z[J], nr[J]), ...);
 }
 
-template <Opt O, int RB, bool Full>
+// ---------------------------------------------------------------------------
+// Packed fast path: elements 2w and 2w+1 in the two lanes of f32x2 operations.
+// Every operation rounds exactly as its scalar counterpart in element_exact;
+// division and square root use the validated sequences of fo_pair.cuh, and
+// `bad` is raised when an operand leaves their validated range.
+// ---------------------------------------------------------------------------
+
+// Per-thread packed constants.
+struct PairConsts {
+    f2 cm;      // s_m / 127 (both lanes)
+    f2 cv;      // s_v / 255
+    f2 ncv23;   // -(2^23 * s_v / 255): (2^23 + q) * cv - 2^23 * cv = q * cv exactly
+    f2 coef;    // per-row decay (AdamW, Lion) or weight decay (SGD)
+};
+
+// theta^ of elements 2w, 2w+1 (see merge_one), packed.
+template <int RB, int W>
+__device__ __forceinline__ f2 merge_pair(const Loaded &L, const uint32_t (&rx)[8])
+{
+    const uint32_t u0 = L.t[W] << 16, u1 = L.t[W] & 0xFFFF0000u;
+    f2 rho;
+    if (RB == 8) {
+        constexpr int b0 = (2 * W) & 3, b1 = (2 * W + 1) & 3;
+        const uint32_t w = rx[(2 * W) >> 2];
+        rho = add2(pk(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | b0)),
+                      __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | b1))),
+                   splat(-8388736.0f));
+    } else {
+        const uint32_t w = rx[W];
+        rho = add2(pk(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7410u)),
+                      __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7432u))),
+                   splat(-8421376.0f));
+    }
+    const f2 t = mul2(rho, splat(RhoConst<RB>::kappa));
+    const f2 nb = fma2(t, splat(32768.0f), splat(kRoundMagic));
+    const f2 zero_case = mul2(t, splat(kTwoPowMinus134));
+    float n0f, n1f, z0, z1;
+    unpk(nb, n0f, n1f);
+    unpk(zero_case, z0, z1);
+    const int n0 = (int)(__float_as_uint(n0f) - kRoundMagicBits);
+    const int n1 = (int)(__float_as_uint(n1f) - kRoundMagicBits);
+    const int s0 = (int)u0 >> 31, s1 = (int)u1 >> 31;
+    const float r0 = __uint_as_float(u0) == 0.0f ? z0 : __uint_as_float(u0 + (uint32_t)((n0 ^ s0) - s0));
+    const float r1 = __uint_as_float(u1) == 0.0f ? z1 : __uint_as_float(u1 + (uint32_t)((n1 ^ s1) - s1));
+    return pk(r0, r1);
+}
+
+// m^ = phi_m^-1(code * s_m/127) of elements 2w, 2w+1, packed.
+template <int W>
+__device__ __forceinline__ f2 mhat_pair(const uint32_t (&mx)[4], const PairConsts &k)
+{
+    constexpr int b0 = (2 * W) & 3, b1 = (2 * W + 1) & 3;
+    const uint32_t w = mx[(2 * W) >> 2];
+    const f2 q = add2(pk(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | b0)),
+                         __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | b1))),
+                      splat(-8388736.0f));
+    const f2 zq = mul2(q, k.cm);
+    float a0, a1;
+    unpk(zq, a0, a1);
+    // |zq| - 2 = -(2 - |zq|): the operands are below 2 in magnitude (scale < 2)
+    return div2(zq, pk(__fsub_rn(fabsf(a0), 2.0f), __fsub_rn(fabsf(a1), 2.0f)));
+}
+
+// z = phi_m(m) = 2m / (1 + |m|), packed.
+__device__ __forceinline__ f2 phi_m_pair(f2 m)
+{
+    float m0, m1;
+    unpk(m, m0, m1);
+    return div2(add2(m, m), pk(__fsub_rn(-fabsf(m0), 1.0f), __fsub_rn(-fabsf(m1), 1.0f)));
+}
+
+__device__ __forceinline__ bool outside(float x, float lo, float hi)
+{
+    return !(fabsf(x) >= lo && fabsf(x) <= hi);
+}
+
+template <Opt O, int RB, int W>
+__device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
+                                          const StepScalars &s, const PairConsts &k,
+                                          float (&th)[kEPT], float (&z)[kEPT], float (&nr)[kEPT], bool &bad)
+{
+    constexpr int j0 = 2 * W, j1 = 2 * W + 1;
+    const f2 g = pk(__uint_as_float(L.g[W] << 16), __uint_as_float(L.g[W] & 0xFFFF0000u));
+    float g0, g1;
+    unpk(g, g0, g1);
+    const f2 theta = merge_pair<RB, W>(L, rx);
+    const f2 mhat = mhat_pair<W>(mx, k);
+    f2 thn, m, nrv = 0;
+
+    if (O == Opt::kAdamW) {
+        // (2^23 + q) as floats -> q * s_v/255 in one fma
+        constexpr int b0 = j0 & 3, b1 = j1 & 3;
+        const uint32_t vw = L.v[j0 >> 2];
+        const f2 rq = fma2(pk(__uint_as_float(__byte_perm(vw, 0x4B000000u, 0x7440u | b0)),
+                              __uint_as_float(__byte_perm(vw, 0x4B000000u, 0x7440u | b1))),
+                           k.cv, k.ncv23);
+        const f2 vhat = mul2(rq, rq);
+        const f2 thd = mul2(theta, k.coef);
+        m = fma2(s.p[0], mhat, mul2(s.p[2], g));                   // b1*m + (1-b1)*g
+        const f2 nv = fma2(s.p[1], vhat, mul2(mul2(s.p[3], g), g)); // -(b2*v + ((1-b2)*g)*g)
+        float v0, v1;
+        unpk(nv, v0, v1);
+        bad |= outside(v0, 0x1p-100f, 0x1p100f) | outside(v1, 0x1p-100f, 0x1p100f);
+        bad |= outside(g0, 0.0f, 0x1p24f) | outside(g1, 0.0f, 0x1p24f);
+        nrv = neg_sqrt2(nv);                                        // -sqrt(v)
+        const f2 nden = fma2(nrv, s.p[4], s.p[5]);                  // -(sqrt(v)/sqrt(bc2) + eps)
+        f2 q0;
+        const f2 u = div2(m, nden, q0);                             // m / den
+        float q00, q01;
+        unpk(q0, q00, q01);
+        bad |= outside(q00, 0x1p-60f, 0x1p80f) | outside(q01, 0x1p-60f, 0x1p80f);
+        thn = fma2(s.p[6], u, thd);                                 // theta - lr/bc1 * m/den
+    } else if (O == Opt::kSgd) {
+        const f2 gp = fma2(k.coef, theta, g);                       // g + wd*theta
+        m = fma2(s.p[0], mhat, gp);                                 // mu*m + g'
+        thn = fma2(s.p[1], m, theta);                               // theta - lr*m
+        float m0, m1;
+        unpk(m, m0, m1);
+        bad |= outside(m0, 0.0f, 0x1p100f) | outside(m1, 0.0f, 0x1p100f);
+    } else {
+        const f2 c = fma2(s.p[0], mhat, mul2(s.p[2], g));           // b1*m + (1-b1)*g
+        float c0, c1;
+        unpk(c, c0, c1);
+        const f2 sgn = pk(c0 > 0.0f ? 1.0f : (c0 < 0.0f ? -1.0f : 0.0f),
+                          c1 > 0.0f ? 1.0f : (c1 < 0.0f ? -1.0f : 0.0f));
+        thn = fma2(s.p[4], sgn, mul2(theta, k.coef));               // theta*(1-lr*wd) - lr*sign(c)
+        m = fma2(s.p[1], mhat, mul2(s.p[3], g));                    // b2*m + (1-b2)*g
+        float m0, m1;
+        unpk(m, m0, m1);
+        bad |= outside(m0, 0.0f, 0x1p100f) | outside(m1, 0.0f, 0x1p100f);
+    }
+    unpk(thn, th[j0], th[j1]);
+    unpk(phi_m_pair(m), z[j0], z[j1]);
+    unpk(nrv, nr[j0], nr[j1]);
+}
+
+template <Opt O, int RB, int... W>
+__device__ __forceinline__ void all_fast(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
+                                         const StepScalars &s, const PairConsts &k,
+                                         float (&th)[kEPT], float (&z)[kEPT], float (&nr)[kEPT], bool &bad,
+                                         std::integer_sequence<int, W...>)
+{
+    (pair_fast<O, RB, W>(L, rx, mx, s, k, th, z, nr, bad), ...);
+}
+
+template <Opt O, int RB>
 __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalars &s, int64_t i0)
 {
     constexpr bool WithV = (O == Opt::kAdamW);
-    int cnt = kEPT;
-    if (!Full) {
-        const int64_t rem = row.numel - i0;
-        cnt = rem >= kEPT ? kEPT : (rem > 0 ? (int)rem : 0);
-    }
+    const int64_t rem = row.numel - i0;
+    const int cnt = rem >= kEPT ? kEPT : (rem > 0 ? (int)rem : 0);
+    const bool even = (threadIdx.x & 1) == 0;
 
     Loaded L;
-    if (Full || cnt == kEPT)
-        load_full<RB, WithV>(row, i0, L);
-    else
-        load_partial<RB, WithV>(row, i0, cnt, L);
+    load_chunk<RB, WithV>(row, i0, cnt, L);
 
     // bias the signed codes once per word for the exact byte -> float unpack
     uint32_t rx[8], mx[4];
@@ -181,12 +328,42 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
     for (int w = 0; w < 4; ++w)
         mx[w] = L.m[w] ^ 0x80808080u;
 
-    const float cm = __fdiv_rn(scale_value(L.ms), 127.0f);
-    const float cv = WithV ? __fdiv_rn(scale_value(L.vs), 255.0f) : 0.0f;
+    // decode steps s/127 (m) and s/255 (v): with v, the even lane of the pair
+    // divides for m and the odd lane for v, and they swap results
+    float cm, cv = 0.0f;
+    if (WithV) {
+        const float own = __fdiv_rn(scale_value(even ? L.ms : L.vs), even ? 127.0f : 255.0f);
+        const float other = __shfl_xor_sync(0xFFFFFFFFu, own, 1);
+        cm = even ? own : other;
+        cv = even ? other : own;
+    } else {
+        cm = __fdiv_rn(scale_value(L.ms), 127.0f);
+    }
 
-    float th[kEPT], z[kEPT], r[kEPT];
-    all_elements<O, RB>(L, rx, mx, s, row.coef, cm, cv, th, z, r,
-                        std::make_integer_sequence<int, kEPT>{});
+    float th[kEPT], z[kEPT], nr[kEPT];
+    // the fast path needs the host's range preconditions and a momentum scale
+    // below 2 (so that 2 - |z| stays positive); otherwise every element of
+    // this thread goes through the exact path
+    bool bad = !s.fast || (L.ms & 0x7FFFu) >= 0x4000u;
+    if (!bad) {
+        PairConsts k;
+        k.cm = splat(cm);
+        k.cv = splat(cv);
+        k.ncv23 = splat(__fmul_rn(cv, -8388608.0f));
+        k.coef = splat(row.coef);
+        all_fast<O, RB>(L, rx, mx, s, k, th, z, nr, bad, std::make_integer_sequence<int, kEPT / 2>{});
+    }
+    if (bad) {
+        // rare: reload (the data is unchanged) and recompute with IEEE operations
+        load_chunk<RB, WithV>(row, i0, cnt, L);
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            rx[w] = L.r[w] ^ (RB == 8 ? 0x80808080u : 0x80008000u);
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+            mx[w] = L.m[w] ^ 0x80808080u;
+        all_exact<O, RB>(L, rx, mx, s, row.coef, cm, cv, th, z, nr, std::make_integer_sequence<int, kEPT>{});
+    }
 
     // re-split theta: theta' (BF16, nearest even) and rho
     uint32_t tp[8], ro[8];
@@ -195,12 +372,7 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
         tp[w] = pack_bf16x2(th[2 * w], th[2 * w + 1]);
         const uint32_t c0 = split_code<RB>(__float_as_uint(th[2 * w]), bf16_lo_bits(tp[w]));
         const uint32_t c1 = split_code<RB>(__float_as_uint(th[2 * w + 1]), bf16_hi_bits(tp[w]));
-        if (RB == 16) {
-            ro[w] = pack_halves(c0, c1);
-        } else {
-            // bytes 2w, 2w+1 of the rho words; assembled below
-            ro[w] = __byte_perm(c0, c1, 0x0040u);
-        }
+        ro[w] = RB == 16 ? pack_halves(c0, c1) : __byte_perm(c0, c1, 0x0040u);
     }
     if (RB == 8) {
 #pragma unroll
@@ -212,34 +384,52 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
     float am = 0.0f, av = 0.0f;
 #pragma unroll
     for (int j = 0; j < kEPT; ++j) {
-        if (Full || j < cnt) {
-            am = fmaxf(am, fabsf(z[j]));
-            if (WithV)
-                av = fmaxf(av, r[j]);
-        }
+        const bool valid = j < cnt;
+        am = fmaxf(am, valid ? fabsf(z[j]) : 0.0f);
+        if (WithV)
+            av = fmaxf(av, valid ? -nr[j] : 0.0f);
     }
     am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
     if (WithV)
         av = fmaxf(av, __shfl_xor_sync(0xFFFFFFFFu, av, 1));
 
     const uint16_t sm_new = scale_of(am);
-    const float mult_m = code_multiplier(scale_value(sm_new), 127.0f);
+    const uint16_t sv_new = WithV ? scale_of(av) : (uint16_t)0;
+    // code multipliers 127/s (m) and 255/s (v), split across the pair likewise
+    float mult_m, mult_v = 0.0f;
+    if (WithV) {
+        const float own = code_multiplier(scale_value(even ? sm_new : sv_new), even ? 127.0f : 255.0f);
+        const float other = __shfl_xor_sync(0xFFFFFFFFu, own, 1);
+        mult_m = even ? own : other;
+        mult_v = even ? other : own;
+    } else {
+        mult_m = code_multiplier(scale_value(sm_new), 127.0f);
+    }
     uint32_t mo[4], vo[4];
 #pragma unroll
-    for (int w = 0; w < 4; ++w)
-        mo[w] = pack_bytes(m_code(z[4 * w], mult_m), m_code(z[4 * w + 1], mult_m),
-                           m_code(z[4 * w + 2], mult_m), m_code(z[4 * w + 3], mult_m));
-    uint16_t sv_new = 0;
+    for (int w = 0; w < 4; ++w) {
+        const f2 xa = mul2(pk(z[4 * w], z[4 * w + 1]), splat(mult_m));
+        const f2 xb = mul2(pk(z[4 * w + 2], z[4 * w + 3]), splat(mult_m));
+        float x0, x1, x2, x3;
+        unpk(xa, x0, x1);
+        unpk(xb, x2, x3);
+        mo[w] = pack_bytes(m_code_of(x0), m_code_of(x1), m_code_of(x2), m_code_of(x3));
+    }
     if (WithV) {
-        sv_new = scale_of(av);
-        const float mult_v = code_multiplier(scale_value(sv_new), 255.0f);
+        // r * (255/s) = (-r) * (-(255/s)), exactly
+        const float nmult_v = -mult_v;
 #pragma unroll
-        for (int w = 0; w < 4; ++w)
-            vo[w] = pack_bytes(v_code(r[4 * w], mult_v), v_code(r[4 * w + 1], mult_v),
-                               v_code(r[4 * w + 2], mult_v), v_code(r[4 * w + 3], mult_v));
+        for (int w = 0; w < 4; ++w) {
+            const f2 xa = mul2(pk(nr[4 * w], nr[4 * w + 1]), splat(nmult_v));
+            const f2 xb = mul2(pk(nr[4 * w + 2], nr[4 * w + 3]), splat(nmult_v));
+            float x0, x1, x2, x3;
+            unpk(xa, x0, x1);
+            unpk(xb, x2, x3);
+            vo[w] = pack_bytes(v_code_of(x0), v_code_of(x1), v_code_of(x2), v_code_of(x3));
+        }
     }
 
-    if (Full || cnt == kEPT) {
+    if (cnt == kEPT) {
         st_stream(row.theta + i0, make_uint4(tp[0], tp[1], tp[2], tp[3]));
         st_stream(row.theta + i0 + 8, make_uint4(tp[4], tp[5], tp[6], tp[7]));
         if (RB == 8) {
@@ -254,28 +444,29 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
     } else {
 #pragma unroll
         for (int j = 0; j < kEPT; ++j) {
-            if (j < cnt) {
-                const int sh16 = 16 * (j & 1), sh8 = 8 * (j & 3);
-                row.theta[i0 + j] = (uint16_t)(tp[j >> 1] >> sh16);
-                if (RB == 8)
-                    static_cast<int8_t *>(row.rho)[i0 + j] = (int8_t)(ro[j >> 2] >> sh8);
-                else
-                    static_cast<int16_t *>(row.rho)[i0 + j] = (int16_t)(ro[j >> 1] >> sh16);
-                row.mq[i0 + j] = (int8_t)(mo[j >> 2] >> sh8);
-                if (WithV)
-                    row.vq[i0 + j] = (uint8_t)(vo[j >> 2] >> sh8);
-            }
+            if (j >= cnt)
+                break;
+            const int sh16 = 16 * (j & 1), sh8 = 8 * (j & 3);
+            row.theta[i0 + j] = (uint16_t)(tp[j >> 1] >> sh16);
+            if (RB == 8)
+                static_cast<int8_t *>(row.rho)[i0 + j] = (int8_t)(ro[j >> 2] >> sh8);
+            else
+                static_cast<int16_t *>(row.rho)[i0 + j] = (int16_t)(ro[j >> 1] >> sh16);
+            row.mq[i0 + j] = (int8_t)(mo[j >> 2] >> sh8);
+            if (WithV)
+                row.vq[i0 + j] = (uint8_t)(vo[j >> 2] >> sh8);
         }
     }
-    if ((threadIdx.x & 1) == 0 && cnt > 0) {
+    if (even && cnt > 0) {
         __stcs(row.ms + (i0 >> 5), sm_new);
         if (WithV)
             __stcs(row.vs + (i0 >> 5), sv_new);
     }
 }
 
-template <Opt O>
-__global__ void __launch_bounds__(kStepThreads)
+// One launch: rows of one rho width (RB), walked tile by tile.
+template <Opt O, int RB>
+__global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
 fo_fused_step_kernel(const __grid_constant__ StepParams p)
 {
     int row = 0;
@@ -284,30 +475,18 @@ fo_fused_step_kernel(const __grid_constant__ StepParams p)
             ++row;
         const int first = row == 0 ? 0 : p.tile_end[row - 1];
         const StepRow &r = p.rows[row];
-        const int64_t e0 = (int64_t)(tile - first) * kStepTile;
-        const int64_t i0 = e0 + (int64_t)threadIdx.x * kEPT;
-        const bool full = e0 + kStepTile <= r.numel;
-        if (r.rho_bits == 8) {
-            if (full)
-                thread_step<O, 8, true>(r, p.s, i0);
-            else
-                thread_step<O, 8, false>(r, p.s, i0);
-        } else {
-            if (full)
-                thread_step<O, 16, true>(r, p.s, i0);
-            else
-                thread_step<O, 16, false>(r, p.s, i0);
-        }
+        const int64_t i0 = (int64_t)(tile - first) * kStepTile + (int64_t)threadIdx.x * kEPT;
+        thread_step<O, RB>(r, p.s, i0);
     }
 }
 
-template <Opt O>
+template <Opt O, int RB>
 int resident_ctas()
 {
     static int cached = 0;
     if (cached == 0) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fo_fused_step_kernel<O>, kStepThreads, 0) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fo_fused_step_kernel<O, RB>, kStepThreads, 0) !=
                 cudaSuccess || n < 1)
             n = 1;
         cached = n;
@@ -315,25 +494,32 @@ int resident_ctas()
     return cached;
 }
 
-}  // namespace
-
-cudaError_t launch_step(Opt opt, const StepParams &p, cudaStream_t stream)
+template <Opt O, int RB>
+cudaError_t launch(const StepParams &p, cudaStream_t stream)
 {
-    int ctas = 0;
-    switch (opt) {
-    case Opt::kAdamW: ctas = resident_ctas<Opt::kAdamW>(); break;
-    case Opt::kSgd: ctas = resident_ctas<Opt::kSgd>(); break;
-    default: ctas = resident_ctas<Opt::kLion>(); break;
-    }
-    const long long want = (long long)sm_count() * ctas;
+    const long long want = (long long)sm_count() * resident_ctas<O, RB>();
     const int grid = (int)(want < p.total_tiles ? want : p.total_tiles);
-    switch (opt) {
-    case Opt::kAdamW: fo_fused_step_kernel<Opt::kAdamW><<<grid, kStepThreads, 0, stream>>>(p); break;
-    case Opt::kSgd: fo_fused_step_kernel<Opt::kSgd><<<grid, kStepThreads, 0, stream>>>(p); break;
-    default: fo_fused_step_kernel<Opt::kLion><<<grid, kStepThreads, 0, stream>>>(p); break;
-    }
+    fo_fused_step_kernel<O, RB><<<grid, kStepThreads, 0, stream>>>(p);
     count_launch();
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_step(Opt opt, int rho_bits, const StepParams &p, cudaStream_t stream)
+{
+    if (rho_bits == 8) {
+        switch (opt) {
+        case Opt::kAdamW: return launch<Opt::kAdamW, 8>(p, stream);
+        case Opt::kSgd: return launch<Opt::kSgd, 8>(p, stream);
+        default: return launch<Opt::kLion, 8>(p, stream);
+        }
+    }
+    switch (opt) {
+    case Opt::kAdamW: return launch<Opt::kAdamW, 16>(p, stream);
+    case Opt::kSgd: return launch<Opt::kSgd, 16>(p, stream);
+    default: return launch<Opt::kLion, 16>(p, stream);
+    }
 }
 
 }  // namespace fo
