@@ -234,10 +234,10 @@ __device__ __forceinline__ f2 phi_m_pair(f2 m)
     return div2(add2(m, m), pk(__fsub_rn(-fabsf(m0), 1.0f), __fsub_rn(-fabsf(m1), 1.0f)));
 }
 
-__device__ __forceinline__ bool outside(float x, float lo, float hi)
-{
-    return !(fabsf(x) >= lo && fabsf(x) <= hi);
-}
+// |x| below lo, or NaN
+__device__ __forceinline__ bool below(float x, float lo) { return !(fabsf(x) >= lo); }
+// |x| above hi, or NaN
+__device__ __forceinline__ bool above(float x, float hi) { return !(fabsf(x) <= hi); }
 
 template <Opt O, int RB, int W>
 __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
@@ -265,15 +265,18 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
         const f2 nv = fma2(s.p[1], vhat, mul2(mul2(s.p[3], g), g)); // -(b2*v + ((1-b2)*g)*g)
         float v0, v1;
         unpk(nv, v0, v1);
-        bad |= outside(v0, 0x1p-100f, 0x1p100f) | outside(v1, 0x1p-100f, 0x1p100f);
-        bad |= outside(g0, 0.0f, 0x1p24f) | outside(g1, 0.0f, 0x1p24f);
+        // sqrt needs v >= 2^-100; |g| <= 2^24 bounds v (below 2^50), |m|
+        // (below 2^25) and so the divisions' operands from above
+        bad |= below(v0, 0x1p-100f) | below(v1, 0x1p-100f);
+        bad |= above(g0, 0x1p24f) | above(g1, 0x1p24f);
         nrv = neg_sqrt2(nv);                                        // -sqrt(v)
         const f2 nden = fma2(nrv, s.p[4], s.p[5]);                  // -(sqrt(v)/sqrt(bc2) + eps)
         f2 q0;
         const f2 u = div2(m, nden, q0);                             // m / den
         float q00, q01;
         unpk(q0, q00, q01);
-        bad |= outside(q00, 0x1p-60f, 0x1p80f) | outside(q01, 0x1p-60f, 0x1p80f);
+        // m/den: a quotient of at least 2^-60 keeps |m| >= 2^-100 (den >= 2^-40)
+        bad |= below(q00, 0x1p-60f) | below(q01, 0x1p-60f);
         thn = fma2(s.p[6], u, thd);                                 // theta - lr/bc1 * m/den
     } else if (O == Opt::kSgd) {
         const f2 gp = fma2(k.coef, theta, g);                       // g + wd*theta
@@ -281,7 +284,7 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
         thn = fma2(s.p[1], m, theta);                               // theta - lr*m
         float m0, m1;
         unpk(m, m0, m1);
-        bad |= outside(m0, 0.0f, 0x1p100f) | outside(m1, 0.0f, 0x1p100f);
+        bad |= above(m0, 0x1p100f) | above(m1, 0x1p100f);
     } else {
         const f2 c = fma2(s.p[0], mhat, mul2(s.p[2], g));           // b1*m + (1-b1)*g
         float c0, c1;
@@ -292,7 +295,7 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
         m = fma2(s.p[1], mhat, mul2(s.p[3], g));                    // b2*m + (1-b2)*g
         float m0, m1;
         unpk(m, m0, m1);
-        bad |= outside(m0, 0.0f, 0x1p100f) | outside(m1, 0.0f, 0x1p100f);
+        bad |= above(m0, 0x1p100f) | above(m1, 0x1p100f);
     }
     unpk(thn, th[j0], th[j1]);
     unpk(phi_m_pair(m), z[j0], z[j1]);
@@ -365,13 +368,25 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
         all_exact<O, RB>(L, rx, mx, s, row.coef, cm, cv, th, z, nr, std::make_integer_sequence<int, kEPT>{});
     }
 
-    // re-split theta: theta' (BF16, nearest even) and rho
+    // re-split theta: theta' (BF16, nearest even) and rho (see split_code;
+    // here the magnitude residual is scaled in a packed fma and theta's sign
+    // is applied to the FP32 value before rounding, as rint is odd)
     uint32_t tp[8], ro[8];
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
         tp[w] = pack_bf16x2(th[2 * w], th[2 * w + 1]);
-        const uint32_t c0 = split_code<RB>(__float_as_uint(th[2 * w]), bf16_lo_bits(tp[w]));
-        const uint32_t c1 = split_code<RB>(__float_as_uint(th[2 * w + 1]), bf16_hi_bits(tp[w]));
+        const uint32_t t0 = __float_as_uint(th[2 * w]), t1 = __float_as_uint(th[2 * w + 1]);
+        const f2 x = fma2(pk(__uint_as_float(t0 - bf16_lo_bits(tp[w]) + kRoundMagicBits),
+                             __uint_as_float(t1 - bf16_hi_bits(tp[w]) + kRoundMagicBits)),
+                          splat(RhoConst<RB>::qscale), splat(-RhoConst<RB>::offset));
+        float x0, x1;
+        unpk(x, x0, x1);
+        const f2 c = add2(pk(__uint_as_float(__float_as_uint(x0) ^ (t0 & 0x80000000u)),
+                             __uint_as_float(__float_as_uint(x1) ^ (t1 & 0x80000000u))),
+                          splat(kRoundMagic));
+        float c0f, c1f;
+        unpk(c, c0f, c1f);
+        const uint32_t c0 = __float_as_uint(c0f), c1 = __float_as_uint(c1f);
         ro[w] = RB == 16 ? pack_halves(c0, c1) : __byte_perm(c0, c1, 0x0040u);
     }
     if (RB == 8) {
@@ -380,14 +395,15 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
             ro[w] = __byte_perm(ro[2 * w], ro[2 * w + 1], 0x5410u);
     }
 
-    // group absmax over this thread's valid elements, then over the pair
+    // group absmax over this thread's elements, then over the pair. Lanes past
+    // the end of the tensor were loaded as zeros and so hold z = 0 and
+    // sqrt(v) = 0 exactly: they leave the maxima unchanged.
     float am = 0.0f, av = 0.0f;
 #pragma unroll
     for (int j = 0; j < kEPT; ++j) {
-        const bool valid = j < cnt;
-        am = fmaxf(am, valid ? fabsf(z[j]) : 0.0f);
+        am = fmaxf(am, fabsf(z[j]));
         if (WithV)
-            av = fmaxf(av, valid ? -nr[j] : 0.0f);
+            av = fmaxf(av, -nr[j]);
     }
     am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
     if (WithV)
@@ -413,7 +429,7 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
         float x0, x1, x2, x3;
         unpk(xa, x0, x1);
         unpk(xb, x2, x3);
-        mo[w] = pack_bytes(m_code_of(x0), m_code_of(x1), m_code_of(x2), m_code_of(x3));
+        mo[w] = pack_bytes(m_code_sat(x0), m_code_sat(x1), m_code_sat(x2), m_code_sat(x3));
     }
     if (WithV) {
         // r * (255/s) = (-r) * (-(255/s)), exactly
@@ -425,7 +441,7 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
             float x0, x1, x2, x3;
             unpk(xa, x0, x1);
             unpk(xb, x2, x3);
-            vo[w] = pack_bytes(v_code_of(x0), v_code_of(x1), v_code_of(x2), v_code_of(x3));
+            vo[w] = pack_bytes(v_code_sat(x0), v_code_sat(x1), v_code_sat(x2), v_code_sat(x3));
         }
     }
 
