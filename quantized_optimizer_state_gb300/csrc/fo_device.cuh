@@ -26,6 +26,8 @@ constexpr float kKappa16 = 0x1.0002p-15f;
 constexpr float kQScale8 = 0x1.fcp-9f;       // 127 / 32768
 constexpr float kQScale16 = 0x1.fffcp-1f;    // 32767 / 32768
 constexpr float kTwoPowMinus134 = 0x1p-134f; // h of a zero theta'
+constexpr float kRcp127 = 0x1.020408p-7f;    // RN(1/127)
+constexpr float kRcp255 = 0x1.010102p-8f;    // RN(1/255)
 
 template <int RB> struct RhoConst;
 template <> struct RhoConst<8> {
@@ -222,14 +224,30 @@ __device__ __forceinline__ uint32_t v_code_sat(float x)
 // Streaming global memory access (touched once: evict-first)
 // ---------------------------------------------------------------------------
 
+#ifndef FO_CACHE_HINT
+#define FO_CACHE_HINT 0
+#endif
 __device__ __forceinline__ uint4 ld_stream(const void *p)
 {
+#if FO_CACHE_HINT == 0
     return __ldcs(reinterpret_cast<const uint4 *>(p));
+#elif FO_CACHE_HINT == 1
+    return *reinterpret_cast<const uint4 *>(p);
+#else
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+#endif
 }
 
 __device__ __forceinline__ void st_stream(void *p, uint4 v)
 {
+#if FO_CACHE_HINT == 0
     __stcs(reinterpret_cast<uint4 *>(p), v);
+#else
+    *reinterpret_cast<uint4 *>(p) = v;
+#endif
 }
 
 }  // namespace fo

@@ -114,4 +114,25 @@ __device__ __forceinline__ f2 neg_sqrt2(f2 nv)
     return fma2(d, h, ns);                    // -(s + (v - s*s)*h)
 }
 
+// RN(a / b) for a constant b with its correctly rounded reciprocal y = RN(1/b)
+// (Markstein's correction step only), valid for a = 0 or |a/b| in
+// [2^-100, 2^100] with a normal.
+__device__ __forceinline__ float div_by_const(float a, float nb, float y)
+{
+    const float q0 = __fmul_rn(a, y);
+    const float r = __fmaf_rn(nb, q0, a);   // a - b*q0, exact
+    return __fmaf_rn(r, y, q0);
+}
+
+// RN(a / b) for a scalar b in [2^-100, 2^100] and a/b in the same range.
+__device__ __forceinline__ float div1(float a, float b)
+{
+    const float y0 = rcp_approx(b);
+    const float e = __fmaf_rn(-b, y0, 1.0f);
+    const float y1 = __fmaf_rn(y0, e, y0);
+    const float q0 = __fmul_rn(a, y1);
+    const float r = __fmaf_rn(-b, q0, a);
+    return __fmaf_rn(r, y1, q0);
+}
+
 }  // namespace fo

@@ -331,17 +331,11 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
     for (int w = 0; w < 4; ++w)
         mx[w] = L.m[w] ^ 0x80808080u;
 
-    // decode steps s/127 (m) and s/255 (v): with v, the even lane of the pair
-    // divides for m and the odd lane for v, and they swap results
-    float cm, cv = 0.0f;
-    if (WithV) {
-        const float own = __fdiv_rn(scale_value(even ? L.ms : L.vs), even ? 127.0f : 255.0f);
-        const float other = __shfl_xor_sync(0xFFFFFFFFu, own, 1);
-        cm = even ? own : other;
-        cv = even ? other : own;
-    } else {
-        cm = __fdiv_rn(scale_value(L.ms), 127.0f);
-    }
+    // decode steps s/127 (m) and s/255 (v): correctly rounded divisions by a
+    // constant through its correctly rounded reciprocal (s is 0 or an FP16
+    // value in [2^-24, 65504], inside the validated range)
+    const float cm = div_by_const(scale_value(L.ms), -127.0f, kRcp127);
+    const float cv = WithV ? div_by_const(scale_value(L.vs), -255.0f, kRcp255) : 0.0f;
 
     float th[kEPT], z[kEPT], nr[kEPT];
     // the fast path needs the host's range preconditions and a momentum scale
@@ -411,16 +405,11 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
 
     const uint16_t sm_new = scale_of(am);
     const uint16_t sv_new = WithV ? scale_of(av) : (uint16_t)0;
-    // code multipliers 127/s (m) and 255/s (v), split across the pair likewise
-    float mult_m, mult_v = 0.0f;
-    if (WithV) {
-        const float own = code_multiplier(scale_value(even ? sm_new : sv_new), even ? 127.0f : 255.0f);
-        const float other = __shfl_xor_sync(0xFFFFFFFFu, own, 1);
-        mult_m = even ? own : other;
-        mult_v = even ? other : own;
-    } else {
-        mult_m = code_multiplier(scale_value(sm_new), 127.0f);
-    }
+    // code multipliers 127/s (m) and 255/s (v), 0 for a zero scale; s is an
+    // FP16 value in [2^-24, 65504], inside the validated division range
+    const float s_m = scale_value(sm_new), s_v = scale_value(sv_new);
+    const float mult_m = s_m > 0.0f ? div1(127.0f, s_m) : 0.0f;
+    const float mult_v = (WithV && s_v > 0.0f) ? div1(255.0f, s_v) : 0.0f;
     uint32_t mo[4], vo[4];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
