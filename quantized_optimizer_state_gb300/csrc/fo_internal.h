@@ -9,7 +9,10 @@ namespace fo {
 
 constexpr int kGroup = 32;           // quantization group (page: G = 32)
 constexpr int kElemsPerThread = 16;  // one thread holds half a group
-constexpr int kStepThreads = 256;
+#ifndef FO_STEP_THREADS
+#define FO_STEP_THREADS 256
+#endif
+constexpr int kStepThreads = FO_STEP_THREADS;
 constexpr int kStepTile = kStepThreads * kElemsPerThread;  // 4096 elements per tile
 
 enum class Opt : int { kAdamW = 0, kSgd = 1, kLion = 2 };

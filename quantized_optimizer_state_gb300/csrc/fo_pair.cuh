@@ -10,14 +10,14 @@
 // (P. Markstein, "Computation of elementary functions on the IBM RISC
 // System/6000 processor", IBM J. Res. Dev. 34(1), 1990; see also Muller et
 // al., "Handbook of Floating-Point Arithmetic", ch. on FMA-based division).
-// Square root (RN(sqrt(v))): one Goldschmidt refinement of s = v*y,
-// h = y/2 from the hardware reciprocal-square-root approximation y, then the
-// exact remainder d = v - s*s and RN(s + d*h) (same references).
+// Square root (RN(sqrt(v))): s = v*y and h = y/2 from the hardware
+// reciprocal-square-root approximation y, the exact remainder d = v - s*s
+// and RN(s + d*h) (the same remainder correction, for square roots).
 //
 // Validity: both sequences were checked bit for bit against the CUDA
 // correctly rounded operations -- the reciprocal over every significand of
 // ten binades from 2^-126 to 2^125, the division over 3.2e9 operand pairs,
-// the square root over every value of twelve binades from 2^-100 to 2^126.
+// the square root over every FP32 value from 2^-100 up.
 // They are used only where the operands are inside the ranges listed at each
 // function; callers check the ranges and recompute elsewhere with the IEEE
 // operations.
@@ -99,17 +99,17 @@ __device__ __forceinline__ f2 div2(f2 a, f2 nb)
     return div2(a, nb, q0);
 }
 
-// -RN(sqrt(v)) in both lanes, given nv = -v with v in [2^-100, 2^126].
+// -RN(sqrt(v)) in both lanes, given nv = -v with v in [2^-100, 2^126]:
+// s = v*y and h = y/2 from the hardware reciprocal square root y, then the
+// exact remainder d = v - s*s and RN(s + d*h) (checked equal to __fsqrt_rn
+// for every FP32 in [2^-100, 2^128)).
 __device__ __forceinline__ f2 neg_sqrt2(f2 nv)
 {
     float v0, v1;
     unpk(nv, v0, v1);
     const f2 y = pk(rsqrt_approx(-v0), rsqrt_approx(-v1));
-    f2 ns = mul2(nv, y);                      // -s, s ~ sqrt(v)
-    f2 h = mul2(splat(0.5f), y);              // h ~ 1/(2 sqrt(v))
-    const f2 e = fma2(ns, h, splat(0.5f));    // 1/2 - s*h
-    ns = fma2(ns, e, ns);                     // -(s + s*e)
-    h = fma2(h, e, h);
+    const f2 ns = mul2(nv, y);                // -s
+    const f2 h = mul2(splat(0.5f), y);
     const f2 d = fma2(ns, ns, nv);            // s*s - v = -(v - s*s), exact
     return fma2(d, h, ns);                    // -(s + (v - s*s)*h)
 }

@@ -26,7 +26,9 @@ constexpr int kEPT = kElemsPerThread;
 #ifndef FO_STEP_MIN_BLOCKS
 #define FO_STEP_MIN_BLOCKS 4
 #endif
+
 constexpr int kStepMinBlocks = FO_STEP_MIN_BLOCKS;
+
 
 struct Loaded {
     uint32_t g[8];   // 16 BF16 gradients
@@ -178,9 +180,12 @@ struct PairConsts {
     f2 coef;    // per-row decay (AdamW, Lion) or weight decay (SGD)
 };
 
-// theta^ of elements 2w, 2w+1 (see merge_one), packed.
+// theta^ of elements 2w, 2w+1 (see merge_one), packed: the pattern of theta'
+// plus sign(theta') * rint(rho*kappa * 2^15), the sign applied through the
+// multiplier +-2^15 of the rounding fma. A zero theta' (whose h is 2^-134
+// instead) raises `bad` for the exact path.
 template <int RB, int W>
-__device__ __forceinline__ f2 merge_pair(const Loaded &L, const uint32_t (&rx)[8])
+__device__ __forceinline__ f2 merge_pair(const Loaded &L, const uint32_t (&rx)[8], bool &bad)
 {
     const uint32_t u0 = L.t[W] << 16, u1 = L.t[W] & 0xFFFF0000u;
     f2 rho;
@@ -197,17 +202,14 @@ __device__ __forceinline__ f2 merge_pair(const Loaded &L, const uint32_t (&rx)[8
                    splat(-8421376.0f));
     }
     const f2 t = mul2(rho, splat(RhoConst<RB>::kappa));
-    const f2 nb = fma2(t, splat(32768.0f), splat(kRoundMagic));
-    const f2 zero_case = mul2(t, splat(kTwoPowMinus134));
-    float n0f, n1f, z0, z1;
+    const f2 mult = pk(__uint_as_float((u0 & 0x80000000u) | 0x47000000u),      // +-2^15
+                       __uint_as_float((u1 & 0x80000000u) | 0x47000000u));
+    const f2 nb = fma2(t, mult, splat(kRoundMagic));    // M + sign * rint(t * 2^15)
+    float n0f, n1f;
     unpk(nb, n0f, n1f);
-    unpk(zero_case, z0, z1);
-    const int n0 = (int)(__float_as_uint(n0f) - kRoundMagicBits);
-    const int n1 = (int)(__float_as_uint(n1f) - kRoundMagicBits);
-    const int s0 = (int)u0 >> 31, s1 = (int)u1 >> 31;
-    const float r0 = __uint_as_float(u0) == 0.0f ? z0 : __uint_as_float(u0 + (uint32_t)((n0 ^ s0) - s0));
-    const float r1 = __uint_as_float(u1) == 0.0f ? z1 : __uint_as_float(u1 + (uint32_t)((n1 ^ s1) - s1));
-    return pk(r0, r1);
+    bad |= (__uint_as_float(u0) == 0.0f) | (__uint_as_float(u1) == 0.0f);
+    return pk(__uint_as_float(u0 + __float_as_uint(n0f) - kRoundMagicBits),
+              __uint_as_float(u1 + __float_as_uint(n1f) - kRoundMagicBits));
 }
 
 // m^ = phi_m^-1(code * s_m/127) of elements 2w, 2w+1, packed.
@@ -248,7 +250,7 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
     const f2 g = pk(__uint_as_float(L.g[W] << 16), __uint_as_float(L.g[W] & 0xFFFF0000u));
     float g0, g1;
     unpk(g, g0, g1);
-    const f2 theta = merge_pair<RB, W>(L, rx);
+    const f2 theta = merge_pair<RB, W>(L, rx, bad);
     const f2 mhat = mhat_pair<W>(mx, k);
     f2 thn, m, nrv = 0;
 
@@ -311,16 +313,19 @@ __device__ __forceinline__ void all_fast(const Loaded &L, const uint32_t (&rx)[8
     (pair_fast<O, RB, W>(L, rx, mx, s, k, th, z, nr, bad), ...);
 }
 
+__device__ __forceinline__ int chunk_count(const StepRow &row, int64_t i0)
+{
+    const int64_t rem = row.numel - i0;
+    return rem >= kEPT ? kEPT : (rem > 0 ? (int)rem : 0);
+}
+
+// One thread's 16 elements of a tile, from data already loaded into L.
 template <Opt O, int RB>
-__device__ __forceinline__ void thread_step(const StepRow &row, const StepScalars &s, int64_t i0)
+__device__ __forceinline__ void thread_step(const StepRow &row, const StepScalars &s, int64_t i0, int cnt,
+                                            Loaded &L)
 {
     constexpr bool WithV = (O == Opt::kAdamW);
-    const int64_t rem = row.numel - i0;
-    const int cnt = rem >= kEPT ? kEPT : (rem > 0 ? (int)rem : 0);
     const bool even = (threadIdx.x & 1) == 0;
-
-    Loaded L;
-    load_chunk<RB, WithV>(row, i0, cnt, L);
 
     // bias the signed codes once per word for the exact byte -> float unpack
     uint32_t rx[8], mx[4];
@@ -474,6 +479,7 @@ template <Opt O, int RB>
 __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
 fo_fused_step_kernel(const __grid_constant__ StepParams p)
 {
+    constexpr bool WithV = (O == Opt::kAdamW);
     int row = 0;
     for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
         while (tile >= p.tile_end[row])
@@ -481,7 +487,10 @@ fo_fused_step_kernel(const __grid_constant__ StepParams p)
         const int first = row == 0 ? 0 : p.tile_end[row - 1];
         const StepRow &r = p.rows[row];
         const int64_t i0 = (int64_t)(tile - first) * kStepTile + (int64_t)threadIdx.x * kEPT;
-        thread_step<O, RB>(r, p.s, i0);
+        const int cnt = chunk_count(r, i0);
+        Loaded L;
+        load_chunk<RB, WithV>(r, i0, cnt, L);
+        thread_step<O, RB>(r, p.s, i0, cnt, L);
     }
 }
 
@@ -492,7 +501,8 @@ int resident_ctas()
     if (cached == 0) {
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fo_fused_step_kernel<O, RB>, kStepThreads, 0) !=
-                cudaSuccess || n < 1)
+                cudaSuccess ||
+            n < 1)
             n = 1;
         cached = n;
     }
