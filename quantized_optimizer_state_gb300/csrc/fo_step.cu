@@ -22,9 +22,10 @@ namespace fo {
 namespace {
 
 constexpr int kEPT = kElemsPerThread;
-// resident CTAs per SM the register budget is sized for (4: 64 registers a thread)
+// resident CTAs per SM the register budget is sized for (3: 80 registers a
+// thread, which the fast path needs without spilling)
 #ifndef FO_STEP_MIN_BLOCKS
-#define FO_STEP_MIN_BLOCKS 4
+#define FO_STEP_MIN_BLOCKS 3
 #endif
 
 constexpr int kStepMinBlocks = FO_STEP_MIN_BLOCKS;
@@ -172,6 +173,26 @@ __device__ __forceinline__ void all_exact(const Loaded &L, const uint32_t (&rx)[
 // `bad` is raised when an operand leaves their validated range.
 // ---------------------------------------------------------------------------
 
+// Running extremes of the fast path's range-checked operands; one check per
+// thread at the end (three-input min/max instead of a compare per element).
+struct Guard {
+    float min_tp;   // smallest |theta'| (0: a zero theta', exact path)
+    float max_nv;   // largest -v (above -2^-100: v too small for the fast sqrt)
+    float min_q;    // smallest |m/den| first quotient (below 2^-60: exact path)
+    float max_a;    // largest |g| (AdamW, bound 2^24) or |m| (SGD, Lion, bound 2^100)
+    __device__ __forceinline__ void init()
+    {
+        min_tp = __int_as_float(0x7F800000);
+        max_nv = -__int_as_float(0x7F800000);
+        min_q = __int_as_float(0x7F800000);
+        max_a = 0.0f;
+    }
+    __device__ __forceinline__ bool failed(float max_a_bound) const
+    {
+        return !(min_tp > 0.0f) | !(max_nv <= -0x1p-100f) | !(min_q >= 0x1p-60f) | !(max_a <= max_a_bound);
+    }
+};
+
 // Per-thread packed constants.
 struct PairConsts {
     f2 cm;      // s_m / 127 (both lanes)
@@ -185,7 +206,7 @@ struct PairConsts {
 // multiplier +-2^15 of the rounding fma. A zero theta' (whose h is 2^-134
 // instead) raises `bad` for the exact path.
 template <int RB, int W>
-__device__ __forceinline__ f2 merge_pair(const Loaded &L, const uint32_t (&rx)[8], bool &bad)
+__device__ __forceinline__ f2 merge_pair(const Loaded &L, const uint32_t (&rx)[8], Guard &gd)
 {
     const uint32_t u0 = L.t[W] << 16, u1 = L.t[W] & 0xFFFF0000u;
     f2 rho;
@@ -201,13 +222,22 @@ __device__ __forceinline__ f2 merge_pair(const Loaded &L, const uint32_t (&rx)[8
                       __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7432u))),
                    splat(-8421376.0f));
     }
-    const f2 t = mul2(rho, splat(RhoConst<RB>::kappa));
-    const f2 mult = pk(__uint_as_float((u0 & 0x80000000u) | 0x47000000u),      // +-2^15
-                       __uint_as_float((u1 & 0x80000000u) | 0x47000000u));
-    const f2 nb = fma2(t, mult, splat(kRoundMagic));    // M + sign * rint(t * 2^15)
+    f2 nb;   // M + sign(theta') * rint(RN(rho*kappa) * 2^15)
+    if (RB == 8) {
+        // for every 8-bit rho, rint(rho*kappa*2^15) with the exact product
+        // equals rint(RN(rho*kappa)*2^15): one fma with +-kappa*2^15
+        const uint32_t kb = __float_as_uint(RhoConst<8>::kappa * 32768.0f);
+        nb = fma2(rho, pk(__uint_as_float((u0 & 0x80000000u) | kb), __uint_as_float((u1 & 0x80000000u) | kb)),
+                  splat(kRoundMagic));
+    } else {
+        const f2 t = mul2(rho, splat(RhoConst<RB>::kappa));
+        nb = fma2(t, pk(__uint_as_float((u0 & 0x80000000u) | 0x47000000u),       // +-2^15
+                        __uint_as_float((u1 & 0x80000000u) | 0x47000000u)),
+                  splat(kRoundMagic));
+    }
     float n0f, n1f;
     unpk(nb, n0f, n1f);
-    bad |= (__uint_as_float(u0) == 0.0f) | (__uint_as_float(u1) == 0.0f);
+    gd.min_tp = fminf(gd.min_tp, fminf(fabsf(__uint_as_float(u0)), fabsf(__uint_as_float(u1))));
     return pk(__uint_as_float(u0 + __float_as_uint(n0f) - kRoundMagicBits),
               __uint_as_float(u1 + __float_as_uint(n1f) - kRoundMagicBits));
 }
@@ -236,21 +266,18 @@ __device__ __forceinline__ f2 phi_m_pair(f2 m)
     return div2(add2(m, m), pk(__fsub_rn(-fabsf(m0), 1.0f), __fsub_rn(-fabsf(m1), 1.0f)));
 }
 
-// |x| below lo, or NaN
-__device__ __forceinline__ bool below(float x, float lo) { return !(fabsf(x) >= lo); }
-// |x| above hi, or NaN
-__device__ __forceinline__ bool above(float x, float hi) { return !(fabsf(x) <= hi); }
+
 
 template <Opt O, int RB, int W>
 __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
                                           const StepScalars &s, const PairConsts &k,
-                                          float (&th)[kEPT], float (&z)[kEPT], float (&nr)[kEPT], bool &bad)
+                                          float (&th)[kEPT], float (&z)[kEPT], float (&nr)[kEPT], Guard &gd)
 {
     constexpr int j0 = 2 * W, j1 = 2 * W + 1;
     const f2 g = pk(__uint_as_float(L.g[W] << 16), __uint_as_float(L.g[W] & 0xFFFF0000u));
     float g0, g1;
     unpk(g, g0, g1);
-    const f2 theta = merge_pair<RB, W>(L, rx, bad);
+    const f2 theta = merge_pair<RB, W>(L, rx, gd);
     const f2 mhat = mhat_pair<W>(mx, k);
     f2 thn, m, nrv = 0;
 
@@ -269,8 +296,8 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
         unpk(nv, v0, v1);
         // sqrt needs v >= 2^-100; |g| <= 2^24 bounds v (below 2^50), |m|
         // (below 2^25) and so the divisions' operands from above
-        bad |= below(v0, 0x1p-100f) | below(v1, 0x1p-100f);
-        bad |= above(g0, 0x1p24f) | above(g1, 0x1p24f);
+        gd.max_nv = fmaxf(gd.max_nv, fmaxf(v0, v1));
+        gd.max_a = fmaxf(gd.max_a, fmaxf(fabsf(g0), fabsf(g1)));
         nrv = neg_sqrt2(nv);                                        // -sqrt(v)
         const f2 nden = fma2(nrv, s.p[4], s.p[5]);                  // -(sqrt(v)/sqrt(bc2) + eps)
         f2 q0;
@@ -278,7 +305,7 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
         float q00, q01;
         unpk(q0, q00, q01);
         // m/den: a quotient of at least 2^-60 keeps |m| >= 2^-100 (den >= 2^-40)
-        bad |= below(q00, 0x1p-60f) | below(q01, 0x1p-60f);
+        gd.min_q = fminf(gd.min_q, fminf(fabsf(q00), fabsf(q01)));
         thn = fma2(s.p[6], u, thd);                                 // theta - lr/bc1 * m/den
     } else if (O == Opt::kSgd) {
         const f2 gp = fma2(k.coef, theta, g);                       // g + wd*theta
@@ -286,7 +313,7 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
         thn = fma2(s.p[1], m, theta);                               // theta - lr*m
         float m0, m1;
         unpk(m, m0, m1);
-        bad |= above(m0, 0x1p100f) | above(m1, 0x1p100f);
+        gd.max_a = fmaxf(gd.max_a, fmaxf(fabsf(m0), fabsf(m1)));
     } else {
         const f2 c = fma2(s.p[0], mhat, mul2(s.p[2], g));           // b1*m + (1-b1)*g
         float c0, c1;
@@ -297,7 +324,7 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
         m = fma2(s.p[1], mhat, mul2(s.p[3], g));                    // b2*m + (1-b2)*g
         float m0, m1;
         unpk(m, m0, m1);
-        bad |= above(m0, 0x1p100f) | above(m1, 0x1p100f);
+        gd.max_a = fmaxf(gd.max_a, fmaxf(fabsf(m0), fabsf(m1)));
     }
     unpk(thn, th[j0], th[j1]);
     unpk(phi_m_pair(m), z[j0], z[j1]);
@@ -307,10 +334,10 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
 template <Opt O, int RB, int... W>
 __device__ __forceinline__ void all_fast(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
                                          const StepScalars &s, const PairConsts &k,
-                                         float (&th)[kEPT], float (&z)[kEPT], float (&nr)[kEPT], bool &bad,
+                                         float (&th)[kEPT], float (&z)[kEPT], float (&nr)[kEPT], Guard &gd,
                                          std::integer_sequence<int, W...>)
 {
-    (pair_fast<O, RB, W>(L, rx, mx, s, k, th, z, nr, bad), ...);
+    (pair_fast<O, RB, W>(L, rx, mx, s, k, th, z, nr, gd), ...);
 }
 
 __device__ __forceinline__ int chunk_count(const StepRow &row, int64_t i0)
@@ -353,7 +380,14 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
         k.cv = splat(cv);
         k.ncv23 = splat(__fmul_rn(cv, -8388608.0f));
         k.coef = splat(row.coef);
-        all_fast<O, RB>(L, rx, mx, s, k, th, z, nr, bad, std::make_integer_sequence<int, kEPT / 2>{});
+        Guard gd;
+        gd.init();
+        if (O != Opt::kAdamW) {   // no v and no m/den: those checks pass trivially
+            gd.max_nv = -1.0f;
+            gd.min_q = 1.0f;
+        }
+        all_fast<O, RB>(L, rx, mx, s, k, th, z, nr, gd, std::make_integer_sequence<int, kEPT / 2>{});
+        bad = gd.failed(O == Opt::kAdamW ? 0x1p24f : 0x1p100f);
     }
     if (bad) {
         // rare: reload (the data is unchanged) and recompute with IEEE operations
