@@ -340,6 +340,23 @@ def _make_step(opt, hp, table):
     return lambda t, s: fo.fo_lion_step(table, hp["lr"], hp["beta1"], hp["beta2"], s)
 
 
+def reduce_scalar(x, op, ws, device=None):
+    """x reduced over the ranks with op ("max" or "sum"); x itself when ws == 1."""
+    if ws == 1 or op is None:
+        return x
+    import torch
+    import torch.distributed as dist
+    rop = {"max": dist.ReduceOp.MAX, "sum": dist.ReduceOp.SUM}.get(op, op)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=rop)
+    return float(t.item())
+
+
+def job_throughput(ws, params_per_rank, steps, elapsed_ms_max):
+    """Whole-job params/s: all ranks' parameters over the slowest rank's time."""
+    return ws * params_per_rank * steps / (elapsed_ms_max * 1e-3)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -357,11 +374,7 @@ def run_ours(args):
             dist.barrier()
 
     def reduce(x, op):
-        if ws == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=op)
-        return float(t.item())
+        return reduce_scalar(x, op, ws, device)
 
     fo.lib()
     w = wl.workload(args.workload, args.rho_bits)
@@ -402,10 +415,10 @@ def run_ours(args):
 
     elapsed_ms = t_all0.elapsed_time(t_all1)
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    elapsed_ms = reduce(elapsed_ms, dist.ReduceOp.MAX if ws > 1 else None)
-    launches_total = int(reduce(float(launches), dist.ReduceOp.SUM if ws > 1 else None))
+    elapsed_ms = reduce(elapsed_ms, "max")
+    launches_total = int(reduce(float(launches), "sum"))
     kernel_ms = statistics.mean(step_ms)     # one library kernel per step on this stream
-    kernel_ms = reduce(kernel_ms, dist.ReduceOp.MAX if ws > 1 else None)
+    kernel_ms = reduce(kernel_ms, "max")
 
     # end to end through the public API with host buffers: per step, the BF16
     # gradients go host -> device from pinned memory and the updated BF16
@@ -423,7 +436,7 @@ def run_ours(args):
         algo = _algo_bytes(w, args.rho_bits) * w.numel
         achieved = algo / (kernel_ms * 1e-3) / 1e9
         out = {
-            "metric": METRIC, "value": ws * w.numel * args.steps / (elapsed_ms * 1e-3), "unit": UNIT,
+            "metric": METRIC, "value": job_throughput(ws, w.numel, args.steps, elapsed_ms), "unit": UNIT,
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -516,9 +529,8 @@ def _e2e(w, states, grads, step_fn_of, stream, device, steps, t, barrier, reduce
     e1.record(stream)
     torch.cuda.synchronize(device)
     barrier()
-    ms = e0.elapsed_time(e1)
-    ms = reduce(ms, dist.ReduceOp.MAX if ws > 1 else None)
-    return {"value": ws * w.numel * steps / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    ms = reduce(e0.elapsed_time(e1), "max")
+    return {"value": job_throughput(ws, w.numel, steps, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps,
             "path": f"pinned host BF16 grads -> device, fo_adamw_step, theta' -> pinned host; "
                     f"{len(chunks)} tensor chunks pipelined on copy-in/compute/copy-out streams"}
