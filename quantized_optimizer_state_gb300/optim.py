@@ -1,0 +1,291 @@
+"""Drop-in PyTorch optimizers over the fused compressed step: FlashAdamW,
+FlashSGD and FlashLion.
+
+"FlashOptim: Optimizers for Memory Efficient Training" presents its
+optimizers as drop-in replacements for the standard ones with unchanged
+hyper-parameters (page sections "创新点和贡献" and "实践建议"). Here each
+parameter's BF16 data *is* theta'; the optimizer keeps the correction rho and
+the companded INT8 momentum (and UINT8 second moment) with their FP16 group
+scales, and one call of the C ABI updates every parameter of a group in one
+kernel launch. Features from the page's practical advice:
+
+* per-group opt-out: ``rho_bits=16`` for a finer master weight, or
+  ``compress=False`` to keep an FP32 master weight and FP32 moments updated by
+  the standard PyTorch optimizer for that group;
+* gradient release: :meth:`attach_grad_release` steps each parameter as soon
+  as its gradient is accumulated and frees the gradient right away;
+* compact checkpoints: :meth:`state_dict` holds theta' (through the model's
+  parameters), rho, codes, scales and the step counters -- about 5 bytes per
+  parameter for AdamW instead of 12;
+* :meth:`master_weights` rebuilds the FP32 master weights.
+
+Parameters must live on a CUDA device: there is no CPU path.
+"""
+from __future__ import annotations
+
+from typing import Callable, Dict, Iterable, List, Optional
+
+import torch
+
+from . import fo
+
+_GROUP = fo.GROUP
+
+
+def _bits16(t: torch.Tensor) -> torch.Tensor:
+    return t.view(torch.int16)
+
+
+class _FlashOptimizer(torch.optim.Optimizer):
+    _kind = ""          # "adamw", "sgd", "lion"
+    _with_v = False
+    _reference = None   # torch optimizer class for compress=False groups
+
+    def __init__(self, params, defaults: Dict):
+        defaults.setdefault("rho_bits", 8)
+        defaults.setdefault("compress", True)
+        super().__init__(params, defaults)
+        self._fallback: Dict[int, torch.optim.Optimizer] = {}
+        for gi, group in enumerate(self.param_groups):
+            if group["rho_bits"] not in (8, 16):
+                raise ValueError("rho_bits must be 8 or 16")
+            for p in group["params"]:
+                if not p.is_cuda:
+                    raise RuntimeError(f"{type(self).__name__} needs CUDA parameters (no CPU path)")
+                if group["compress"]:
+                    self._init_compressed(p, group)
+            if not group["compress"]:
+                self._fallback[gi] = self._make_reference(group)
+
+    # -- state ------------------------------------------------------------
+
+    def _init_compressed(self, p: torch.Tensor, group: Dict) -> None:
+        """theta', rho = split(FP32 weights) (rho = 0 for weights that are BF16
+        already); moments start at zero codes with zero scales."""
+        if not p.is_contiguous():
+            raise ValueError("parameters must be contiguous")
+        n = p.numel()
+        rb = group["rho_bits"]
+        rho = torch.zeros(n, dtype=torch.int16 if rb == 16 else torch.int8, device=p.device)
+        if p.dtype == torch.float32:
+            master = p.detach().reshape(-1).contiguous()
+            tp = torch.empty(n, dtype=torch.bfloat16, device=p.device)
+            fo.fo_split(master, _bits16(tp), rho, rb)
+            p.data = tp.view(p.shape)
+        elif p.dtype != torch.bfloat16:
+            raise TypeError("parameters must be float32 (split on first use) or bfloat16")
+        ng = (n + _GROUP - 1) // _GROUP
+        st = self.state[p]
+        st["step"] = torch.zeros((), dtype=torch.int64)
+        st["rho"] = rho
+        st["m_q"] = torch.zeros(n, dtype=torch.int8, device=p.device)
+        st["m_scale"] = torch.zeros(ng, dtype=torch.int16, device=p.device)
+        if self._with_v:
+            st["v_q"] = torch.zeros(n, dtype=torch.uint8, device=p.device)
+            st["v_scale"] = torch.zeros(ng, dtype=torch.int16, device=p.device)
+
+    def _make_reference(self, group: Dict) -> torch.optim.Optimizer:
+        hp = {k: v for k, v in group.items() if k not in ("params", "rho_bits", "compress")}
+        for p in group["params"]:
+            if p.dtype != torch.float32:
+                raise TypeError("compress=False groups keep FP32 parameters")
+        return self._reference(group["params"], **self._reference_args(hp))
+
+    def _row(self, p: torch.Tensor, group: Dict) -> fo.FoTensor:
+        st = self.state[p]
+        g = p.grad
+        if g.dtype != torch.bfloat16:
+            g = g.to(torch.bfloat16)
+        if not g.is_contiguous():
+            g = g.contiguous()
+        st["_grad_keepalive"] = g
+        return fo.row(_bits16(p.data), st["rho"], st["m_q"], st["m_scale"], _bits16(g),
+                      st.get("v_q"), st.get("v_scale"), self._weight_decay(group),
+                      group["rho_bits"], p.numel())
+
+    def _weight_decay(self, group: Dict) -> float:
+        return float(group.get("weight_decay", 0.0))
+
+    # -- stepping ---------------------------------------------------------
+
+    @torch.no_grad()
+    def step(self, closure: Optional[Callable] = None):
+        loss = None
+        if closure is not None:
+            with torch.enable_grad():
+                loss = closure()
+        for gi, group in enumerate(self.param_groups):
+            if not group["compress"]:
+                self._fallback[gi].step()
+                continue
+            params = [p for p in group["params"] if p.grad is not None]
+            self._step_params(params, group)
+        return loss
+
+    def _step_params(self, params: List[torch.Tensor], group: Dict) -> None:
+        if not params:
+            return
+        # parameters of a group that have taken the same number of steps share a call
+        by_step: Dict[int, List[torch.Tensor]] = {}
+        for p in params:
+            st = self.state[p]
+            st["step"] += 1
+            by_step.setdefault(int(st["step"]), []).append(p)
+        for t, ps in by_step.items():
+            table = fo.Table([self._row(p, group) for p in ps])
+            self._launch(table, group, t)
+            for p in ps:
+                self.state[p].pop("_grad_keepalive", None)
+
+    def _launch(self, table: fo.Table, group: Dict, t: int) -> None:
+        raise NotImplementedError
+
+    # -- gradient release ---------------------------------------------------
+
+    def attach_grad_release(self, params: Optional[Iterable[torch.Tensor]] = None) -> List:
+        """Step each compressed parameter as soon as its gradient has been
+        accumulated and drop the gradient, so that at most one gradient per
+        parameter is alive during backward (no gradient accumulation across
+        backward passes). Returns the hook handles."""
+        handles = []
+        groups = {id(p): g for g in self.param_groups for p in g["params"]}
+        wanted = None if params is None else {id(p) for p in params}
+        for p_id, group in groups.items():
+            if not group["compress"]:
+                continue
+            for p in group["params"]:
+                if id(p) != p_id or (wanted is not None and p_id not in wanted):
+                    continue
+
+                def hook(param, group=group):
+                    with torch.no_grad():
+                        self._step_params([param], group)
+                    param.grad = None
+
+                handles.append(p.register_post_accumulate_grad_hook(hook))
+        return handles
+
+    # -- checkpoints ----------------------------------------------------------
+
+    _COMPRESSED = ("rho", "m_q", "m_scale", "v_q", "v_scale")
+
+    def load_state_dict(self, state_dict: Dict) -> None:
+        """Load a state_dict written by state_dict(). The compressed buffers keep
+        their integer dtypes (torch's loader would cast every state tensor of a
+        floating-point parameter to the parameter's dtype)."""
+        saved = state_dict["state"]
+        kept = {}
+        plain = {}
+        for k, st in saved.items():
+            kept[k] = {n: v for n, v in st.items() if n in self._COMPRESSED}
+            plain[k] = {n: v for n, v in st.items() if n not in self._COMPRESSED}
+        super().load_state_dict({"state": plain, "param_groups": state_dict["param_groups"]})
+        saved_ids = [i for g in state_dict["param_groups"] for i in g["params"]]
+        params = [p for g in self.param_groups for p in g["params"]]
+        for sid, p in zip(saved_ids, params):
+            for n, v in kept.get(sid, {}).items():
+                cur = self.state[p].get(n)
+                if cur is not None and (cur.dtype != v.dtype or cur.shape != v.shape):
+                    raise ValueError(f"state '{n}' does not match the parameter's layout")
+                self.state[p][n] = v.to(device=p.device).clone()
+
+    # -- export ---------------------------------------------------------------
+
+    @torch.no_grad()
+    def master_weights(self) -> Dict[torch.Tensor, torch.Tensor]:
+        """FP32 master weights theta^ = merge(theta', rho) of every compressed parameter."""
+        out = {}
+        for group in self.param_groups:
+            if not group["compress"]:
+                continue
+            for p in group["params"]:
+                w = torch.empty(p.numel(), dtype=torch.float32, device=p.device)
+                fo.fo_merge(_bits16(p.data.reshape(-1)), self.state[p]["rho"], w, group["rho_bits"])
+                out[p] = w.view(p.shape)
+        return out
+
+    def state_bytes(self) -> int:
+        """Bytes held by the compressed optimizer state (rho, codes, scales)."""
+        n = 0
+        for st in self.state.values():
+            for k, v in st.items():
+                if isinstance(v, torch.Tensor) and k != "step":
+                    n += v.numel() * v.element_size()
+        return n
+
+
+class FlashAdamW(_FlashOptimizer):
+    """AdamW (decoupled weight decay) with compressed master weight and state."""
+    _kind = "adamw"
+    _with_v = True
+    _reference = torch.optim.AdamW
+
+    def __init__(self, params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01,
+                 rho_bits=8, compress=True):
+        super().__init__(params, dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay,
+                                      rho_bits=rho_bits, compress=compress))
+
+    @staticmethod
+    def _reference_args(hp):
+        return dict(lr=hp["lr"], betas=hp["betas"], eps=hp["eps"], weight_decay=hp["weight_decay"])
+
+    def _launch(self, table, group, t):
+        b1, b2 = group["betas"]
+        fo.fo_adamw_step(table, group["lr"], b1, b2, group["eps"], t)
+
+
+class FlashSGD(_FlashOptimizer):
+    """SGD with momentum (dampening 0, no Nesterov, L2 weight decay)."""
+    _kind = "sgd"
+    _reference = torch.optim.SGD
+
+    def __init__(self, params, lr=0.1, momentum=0.9, weight_decay=0.0, rho_bits=8, compress=True):
+        super().__init__(params, dict(lr=lr, momentum=momentum, weight_decay=weight_decay,
+                                      rho_bits=rho_bits, compress=compress))
+
+    @staticmethod
+    def _reference_args(hp):
+        return dict(lr=hp["lr"], momentum=hp["momentum"], weight_decay=hp["weight_decay"])
+
+    def _launch(self, table, group, t):
+        fo.fo_sgd_step(table, group["lr"], group["momentum"])
+
+
+class _ReferenceLion(torch.optim.Optimizer):
+    """Uncompressed Lion (FP32 state) for compress=False groups."""
+
+    def __init__(self, params, lr=1e-4, betas=(0.9, 0.99), weight_decay=0.0):
+        super().__init__(params, dict(lr=lr, betas=betas, weight_decay=weight_decay))
+
+    @torch.no_grad()
+    def step(self):
+        for group in self.param_groups:
+            b1, b2 = group["betas"]
+            for p in group["params"]:
+                if p.grad is None:
+                    continue
+                st = self.state[p]
+                if "m" not in st:
+                    st["m"] = torch.zeros_like(p)
+                m = st["m"]
+                c = m.mul(b1).add_(p.grad, alpha=1 - b1)
+                p.mul_(1 - group["lr"] * group["weight_decay"]).add_(torch.sign(c), alpha=-group["lr"])
+                m.mul_(b2).add_(p.grad, alpha=1 - b2)
+
+
+class FlashLion(_FlashOptimizer):
+    """Lion (Chen et al. 2023) with decoupled weight decay."""
+    _kind = "lion"
+    _reference = _ReferenceLion
+
+    def __init__(self, params, lr=1e-4, betas=(0.9, 0.99), weight_decay=0.0, rho_bits=8, compress=True):
+        super().__init__(params, dict(lr=lr, betas=betas, weight_decay=weight_decay,
+                                      rho_bits=rho_bits, compress=compress))
+
+    @staticmethod
+    def _reference_args(hp):
+        return dict(lr=hp["lr"], betas=hp["betas"], weight_decay=hp["weight_decay"])
+
+    def _launch(self, table, group, t):
+        b1, b2 = group["betas"]
+        fo.fo_lion_step(table, group["lr"], b1, b2)

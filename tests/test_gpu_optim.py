@@ -1,0 +1,154 @@
+"""Drop-in optimizers (FlashAdamW, FlashSGD, FlashLion) over the C ABI.
+
+They must produce exactly the oracle's compressed step (page sections
+"融合优化器步骤" and "实践建议": drop-in, per-layer opt-out, gradient
+release, compact checkpoints).
+"""
+import copy
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_optimizer_state_gb300 import optim
+from quantized_optimizer_state_gb300 import workloads as wl
+from tests.gpu_helpers import assert_state_matches
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    oracle.build()
+
+
+SHAPES = [(64, 33), (33,), (128, 256), (1000,)]
+
+
+def _params(seed):
+    g = torch.Generator().manual_seed(seed)
+    return [torch.nn.Parameter((torch.randn(s, generator=g) * 0.02).cuda()) for s in SHAPES]
+
+
+def _oracle_states(params_fp32, rho_bits, with_v, wd):
+    return [oracle.State.from_fp32(p.detach().cpu().numpy().reshape(-1), rho_bits, with_v, wd)
+            for p in params_fp32]
+
+
+def _device_view(opt, p):
+    st = opt.state[p]
+    rho = st["rho"].cpu().numpy()
+    return oracle.State(p.data.view(torch.int16).cpu().numpy().reshape(-1).view(np.uint16), rho,
+                        st["m_q"].cpu().numpy(), st["m_scale"].cpu().numpy().view(np.uint16),
+                        None if "v_q" not in st else st["v_q"].cpu().numpy(),
+                        None if "v_scale" not in st else st["v_scale"].cpu().numpy().view(np.uint16),
+                        0.0, 16 if rho.dtype == np.int16 else 8)
+
+
+@pytest.mark.parametrize("kind,rho_bits", [("adamw", 8), ("adamw", 16), ("sgd", 8), ("lion", 8)])
+def test_optimizer_matches_oracle(kind, rho_bits):
+    params = _params(1)
+    master0 = [p.detach().clone() for p in params]
+    if kind == "adamw":
+        opt = optim.FlashAdamW(params, lr=1e-3, weight_decay=0.01, rho_bits=rho_bits)
+    elif kind == "sgd":
+        opt = optim.FlashSGD(params, lr=0.1, momentum=0.9, weight_decay=1e-4, rho_bits=rho_bits)
+    else:
+        opt = optim.FlashLion(params, lr=1e-4, weight_decay=0.01, rho_bits=rho_bits)
+    wd = {"adamw": 0.01, "sgd": 1e-4, "lion": 0.01}[kind]
+    ref = _oracle_states(master0, rho_bits, kind == "adamw", wd)
+    for p, r in zip(params, ref):           # split at construction
+        assert p.dtype == torch.bfloat16
+        assert np.array_equal(p.data.view(torch.int16).cpu().numpy().reshape(-1).view(np.uint16), r.theta_p)
+    rng = np.random.default_rng(2)
+    for t in range(1, 4):
+        grads = [wl.to_bf16_bits((rng.standard_normal(p.numel()) * 1e-3).astype(np.float32)) for p in params]
+        for p, gb in zip(params, grads):
+            p.grad = torch.from_numpy(gb.view(np.int16)).cuda().view(torch.bfloat16).view(p.shape)
+        opt.step()
+        if kind == "adamw":
+            oracle.adamw_step(ref, grads, 1e-3, 0.9, 0.999, 1e-8, t)
+        elif kind == "sgd":
+            oracle.sgd_step(ref, grads, 0.1, 0.9)
+        else:
+            oracle.lion_step(ref, grads, 1e-4, 0.9, 0.99)
+        torch.cuda.synchronize()
+        for p, r in zip(params, ref):
+            assert_state_matches(_device_view(opt, p), r, f"{kind} step {t}")
+    mw = opt.master_weights()
+    for p, r in zip(params, ref):
+        assert np.array_equal(mw[p].cpu().numpy().reshape(-1), oracle.merge(r.theta_p, r.rho, rho_bits))
+
+
+def _model(seed):
+    torch.manual_seed(seed)
+    return torch.nn.Sequential(torch.nn.Linear(48, 96), torch.nn.GELU(), torch.nn.Linear(96, 7)).cuda()
+
+
+def _train(model, opt, steps, release):
+    g = torch.Generator(device="cuda").manual_seed(5)
+    if release:
+        opt.attach_grad_release()
+    for _ in range(steps):
+        x = torch.randn(64, 48, device="cuda", generator=g).to(torch.bfloat16)
+        loss = model(x).float().square().mean()
+        loss.backward()
+        if not release:
+            opt.step()
+            opt.zero_grad(set_to_none=True)
+    torch.cuda.synchronize()
+
+
+def test_gradient_release_matches_plain_step():
+    a, b = _model(3), _model(3)
+    oa = optim.FlashAdamW(a.parameters(), lr=1e-3)
+    ob = optim.FlashAdamW(b.parameters(), lr=1e-3)
+    _train(a, oa, 4, release=False)
+    _train(b, ob, 4, release=True)
+    for pa, pb in zip(a.parameters(), b.parameters()):
+        assert torch.equal(pa.data, pb.data)
+        assert pb.grad is None
+        for k in ("rho", "m_q", "m_scale", "v_q", "v_scale"):
+            assert torch.equal(oa.state[pa][k], ob.state[pb][k])
+
+
+def test_checkpoint_resume_is_bit_identical():
+    a = _model(4)
+    oa = optim.FlashAdamW(a.parameters(), lr=1e-3)
+    _train(a, oa, 2, release=False)
+    ckpt = {"model": {k: v.clone() for k, v in a.state_dict().items()},
+            "opt": copy.deepcopy(oa.state_dict())}
+    # compact: theta' (BF16) + rho + codes + scales, about 5 B per parameter
+    n = sum(p.numel() for p in a.parameters())
+    model_bytes = sum(v.numel() * v.element_size() for v in ckpt["model"].values())
+    assert model_bytes == 2 * n
+    assert oa.state_bytes() <= 3.125 * n + 64 * 6
+    _train(a, oa, 3, release=False)
+    b = _model(99)
+    b.load_state_dict(ckpt["model"])
+    ob = optim.FlashAdamW(b.parameters(), lr=1e-3)
+    ob.load_state_dict(ckpt["opt"])
+    _train(b, ob, 3, release=False)
+    for pa, pb in zip(a.parameters(), b.parameters()):
+        assert torch.equal(pa.data, pb.data)
+
+
+def test_uncompressed_group_is_standard_adamw():
+    torch.manual_seed(7)
+    w1 = torch.nn.Parameter(torch.randn(300, device="cuda") * 0.02)
+    w2 = torch.nn.Parameter(torch.randn(300, device="cuda") * 0.02)
+    ref = torch.nn.Parameter(w2.detach().clone())
+    opt = optim.FlashAdamW([{"params": [w1]}, {"params": [w2], "compress": False}], lr=1e-3)
+    topt = torch.optim.AdamW([ref], lr=1e-3, weight_decay=0.01)
+    for _ in range(3):
+        g = torch.randn(300, device="cuda") * 1e-3
+        w1.grad = g.to(torch.bfloat16)
+        w2.grad = g.clone()
+        ref.grad = g.clone()
+        opt.step()
+        topt.step()
+    assert w2.dtype == torch.float32 and torch.equal(w2.data, ref.data)
+    assert w1.dtype == torch.bfloat16
