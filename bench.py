@@ -33,8 +33,9 @@ if ROOT not in sys.path:
 METRIC = "FlashAdamW step params/s and achieved HBM GB/s vs ~8 TB/s (1xGB300)"
 UNIT = "params/s"
 # bytes one FlashAdamW step must move per parameter (each byte once):
-# read grad 2 + theta' 2 + rho 1 + m 1 + v 1 + 2 FP16 scales / 32, write all but grad
-ALGO_BYTES_PER_PARAM = {8: 12.25, 16: 14.25}
+# read grad 2 + theta' 2 + rho 1 + m 1 + v 1 + 2 FP16 scales / 32, write all but
+# grad: 12.25 (8-bit rho), 14.25 (16-bit); an FP32 gradient reads 2 more
+GRAD_BYTES = {"bf16": 2, "f32": 4}
 FALLBACK_HBM_GBS = 6800.0
 CPU_SAMPLE_ROWS = ("layers.0.input_layernorm.weight", "layers.0.post_attention_layernorm.weight",
                    "layers.0.self_attn.q_proj.weight", "layers.0.self_attn.k_proj.weight",
@@ -49,6 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="llama31_8b")
     p.add_argument("--rho-bits", type=int, default=8, choices=(8, 16))
+    p.add_argument("--grad-dtype", default="bf16", choices=tuple(GRAD_BYTES),
+                   help="gradient element type the fused step reads")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="time budget of the CPU oracle baseline sample")
@@ -64,27 +67,34 @@ def _dist_env():
     return ws, rank, local
 
 
-def _config(w, rho_bits, n_gpus):
+def _config(w, rho_bits, n_gpus, grad_dtype="bf16"):
+    gname = grad_dtype.upper().replace("F32", "FP32")
     return {
         "workload": f"{w.name}: {len(w.params)} tensors, {w.numel} params, Flash{w.optimizer}"
                     f" step (BF16 theta' + INT{rho_bits} rho + INT8 m"
-                    f"{' + UINT8 v' if w.optimizer == 'adamw' else ''}, G=32 FP16 scales)",
+                    f"{' + UINT8 v' if w.optimizer == 'adamw' else ''}, G=32 FP16 scales,"
+                    f" {gname} grads)",
         "params": w.numel,
         "tensors": len(w.params),
         "optimizer": w.optimizer,
         "rho_bits": rho_bits,
+        "grad_dtype": grad_dtype,
         "hparams": w.hparams,
-        "algorithmic_bytes_per_param": _algo_bytes(w, rho_bits),
-        "l2": "inputs larger than L2 (each step streams ~%.0f GB)" % (w.numel * _algo_bytes(w, rho_bits) / 1e9),
-        "grads": "one seeded synthetic BF16 gradient set, reused every step",
+        "algorithmic_bytes_per_param": _algo_bytes(w, rho_bits, grad_dtype),
+        "l2": "inputs larger than L2 (each step streams ~%.0f GB)"
+              % (w.numel * _algo_bytes(w, rho_bits, grad_dtype) / 1e9),
+        "grads": f"one seeded synthetic {gname} gradient set, reused every step",
         "parallelism": "replicas" if n_gpus > 1 else "single GPU",
     }
 
 
-def _algo_bytes(w, rho_bits):
+def _algo_bytes(w, rho_bits, grad_dtype="bf16"):
+    """Read and write theta' (2), rho (1 or 2), m (1), v (1, AdamW) and their FP16
+    group scales (2/32 each); read the gradient."""
+    state = 2 + rho_bits // 8 + 1 + 2 / 32
     if w.optimizer == "adamw":
-        return ALGO_BYTES_PER_PARAM[rho_bits]
-    return 2 * (2 + rho_bits // 8 + 1 + 2 / 32) + 2
+        state += 1 + 2 / 32
+    return 2 * state + GRAD_BYTES[grad_dtype]
 
 
 # ---------------------------------------------------------------------------
@@ -102,7 +112,7 @@ class OracleSample:
     """Host state of a few rows of the workload, cut into group-aligned chunks
     that the oracle steps on parallel threads (the oracle itself is untouched)."""
 
-    def __init__(self, w, rho_bits, chunk=1 << 20):
+    def __init__(self, w, rho_bits, grad_dtype="bf16", chunk=1 << 20):
         import numpy as np
         import oracle
         from quantized_optimizer_state_gb300 import workloads as wl
@@ -115,7 +125,7 @@ class OracleSample:
             p = w.params[i]
             st = oracle.State.from_fp32(wl.init_weight(p, i), rho_bits, with_v,
                                         w.hparams["weight_decay"])
-            g = wl.grad_bf16(w.grad, w.grad_scale, p.numel, i, 1)
+            g = (wl.grad_fp32 if grad_dtype == "f32" else wl.grad_bf16)(w.grad, w.grad_scale, p.numel, i, 1)
             self.states.append(st)
             self.grads.append(g)
             for lo in range(0, p.numel, chunk):
@@ -148,8 +158,8 @@ class OracleSample:
         self.pool.shutdown()
 
 
-def cpu_baseline(w, rho_bits, seconds):
-    s = OracleSample(w, rho_bits)
+def cpu_baseline(w, rho_bits, seconds, grad_dtype="bf16"):
+    s = OracleSample(w, rho_bits, grad_dtype)
     s.step(1)                                   # warm-up
     t0 = time.perf_counter()
     steps = 0
@@ -170,7 +180,7 @@ def run_reference(args):
         return 0
     from quantized_optimizer_state_gb300 import workloads as wl
     w = wl.workload(args.workload, args.rho_bits)
-    s = OracleSample(w, args.rho_bits)
+    s = OracleSample(w, args.rho_bits, args.grad_dtype)
     for t in range(1, args.warmup + 1):
         s.step(t)
     t0 = time.perf_counter()
@@ -183,7 +193,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": _config(w, args.rho_bits, ws),
+        "data": "synthetic", "config": _config(w, args.rho_bits, ws, args.grad_dtype),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": s.threads, "kind": "oracle",
                          "sample": f"each step: {s.desc}"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -276,10 +286,10 @@ def _kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def _profiled_traffic(workload: str, rho_bits: int):
+def _profiled_traffic(workload: str, rho_bits: int, grad_dtype: str = "bf16"):
     """DRAM bytes per launch from the committed ncu capture of the default
     workload, or None when the kernel sources changed since that capture."""
-    if workload != "llama31_8b" or rho_bits != 8:
+    if workload != "llama31_8b" or rho_bits != 8 or grad_dtype != "bf16":
         return None
     try:
         text = open(PROFILE).read()
@@ -303,7 +313,7 @@ def _measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _build_states(w, rho_bits, device):
+def _build_states(w, rho_bits, device, grad_dtype="bf16"):
     import torch
     from quantized_optimizer_state_gb300 import fo
     from quantized_optimizer_state_gb300 import workloads as wl
@@ -315,7 +325,8 @@ def _build_states(w, rho_bits, device):
         d.init_from(theta)
         del theta
         states.append(d)
-        grads.append(wl.grad_bf16_device(w.grad, w.grad_scale, p.numel, i, 1, device))
+        gen = wl.grad_fp32_device if grad_dtype == "f32" else wl.grad_bf16_device
+        grads.append(gen(w.grad, w.grad_scale, p.numel, i, 1, device))
     torch.cuda.synchronize(device)
     return states, grads
 
@@ -378,7 +389,7 @@ def run_ours(args):
 
     fo.lib()
     w = wl.workload(args.workload, args.rho_bits)
-    states, grads = _build_states(w, args.rho_bits, device)
+    states, grads = _build_states(w, args.rho_bits, device, args.grad_dtype)
     table = fo.table_of(states, grads)
     step = _stepper(w, table)
     stream = torch.cuda.current_stream(device)
@@ -429,20 +440,20 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.rho_bits, args.cpu_seconds)
+        cpu = cpu_baseline(w, args.rho_bits, args.cpu_seconds, args.grad_dtype)
 
     if rank == 0:
         peak, peak_kind = _measured_peak()
-        algo = _algo_bytes(w, args.rho_bits) * w.numel
+        algo = _algo_bytes(w, args.rho_bits, args.grad_dtype) * w.numel
         achieved = algo / (kernel_ms * 1e-3) / 1e9
         out = {
             "metric": METRIC, "value": job_throughput(ws, w.numel, args.steps, elapsed_ms), "unit": UNIT,
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": _config(w, args.rho_bits, ws),
+            "config": _config(w, args.rho_bits, ws, args.grad_dtype),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": _profiled_traffic(args.workload, args.rho_bits),
+                         "frac": achieved / peak, "traffic": _profiled_traffic(args.workload, args.rho_bits, args.grad_dtype),
                          "kernel": f"fo_fused_step_kernel<{w.optimizer}>",
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s",
@@ -487,7 +498,7 @@ def _e2e(w, states, grads, step_fn_of, stream, device, steps, t, barrier, reduce
     offs = [0]
     for n in sizes:
         offs.append(offs[-1] + n)
-    h_grad = torch.empty(offs[-1], dtype=torch.bfloat16, pin_memory=True)
+    h_grad = torch.empty(offs[-1], dtype=grads[0].dtype, pin_memory=True)
     h_out = torch.empty(offs[-1], dtype=torch.int16, pin_memory=True)
     for i, g in enumerate(grads):
         h_grad[offs[i]:offs[i + 1]].copy_(g)
@@ -496,7 +507,7 @@ def _e2e(w, states, grads, step_fn_of, stream, device, steps, t, barrier, reduce
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev_in = [torch.cuda.Event() for _ in chunks]
     ev_done = [torch.cuda.Event() for _ in chunks]
-    h2d = sum(2 * g.numel() for g in grads)
+    h2d = sum(g.element_size() * g.numel() for g in grads)
     d2h = sum(2 * s.numel for s in states)
 
     def one(t):
@@ -532,7 +543,8 @@ def _e2e(w, states, grads, step_fn_of, stream, device, steps, t, barrier, reduce
     ms = reduce(e0.elapsed_time(e1), "max")
     return {"value": job_throughput(ws, w.numel, steps, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps,
-            "path": f"pinned host BF16 grads -> device, fo_adamw_step, theta' -> pinned host; "
+            "path": f"pinned host {str(grads[0].dtype).split('.')[-1]} grads -> device, fused step,"
+                    f" theta' -> pinned host; "
                     f"{len(chunks)} tensor chunks pipelined on copy-in/compute/copy-out streams"}
 
 

@@ -33,6 +33,7 @@
  *   SGD:    m = fma(mu, m, fma(wd, theta, g)); theta = fma(-lr, m, theta).
  *   Lion:   c = fma(b1, m, (1-b1)*g); theta = fma(-lr, sign(c), theta*(1-lr*wd));
  *           m = fma(b2, m, (1-b2)*g).
+ *   g is the row's gradient as FP32 (a BF16 gradient widened exactly).
  *   All arithmetic is IEEE binary32 round-to-nearest-even without flush to
  *   zero. Hyper-parameters are doubles; each per-element scalar is the
  *   hyper-parameter, or a quantity formed from them in double, rounded to FP32.
@@ -93,6 +94,18 @@ typedef enum fo_state_kind {
 typedef void *fo_stream_t;
 
 /*
+ * Element type of a row's gradient. BF16 is the page's setting (the fused
+ * step reads 2 bytes of gradient per parameter). FP32 serves callers whose
+ * gradients are FP32 (for example accumulated in FP32): the FP32 value enters
+ * the FP32 update as it is, with no rounding to BF16 first, at 2 more bytes
+ * of reads per parameter.
+ */
+typedef enum fo_grad_dtype {
+    FO_GRAD_BF16 = 0, /* grad holds uint16_t BF16 bit patterns */
+    FO_GRAD_F32 = 1   /* grad holds float                      */
+} fo_grad_dtype_t;
+
+/*
  * One row of the multi-tensor parameter table: the compressed state of one
  * tensor of numel elements. All pointers are device memory.
  */
@@ -103,11 +116,11 @@ typedef struct fo_tensor {
     uint16_t *m_scale;     /* FP16 momentum scales, ceil(numel/32), in/out             */
     uint8_t *v_q;          /* second-moment codes, numel, in/out (AdamW; else NULL)     */
     uint16_t *v_scale;     /* FP16 second-moment scales (AdamW; else NULL)              */
-    const uint16_t *grad;  /* BF16 gradient, numel, read only                          */
+    const void *grad;      /* gradient, numel, read only; element type per grad_dtype  */
     int64_t numel;         /* elements; 0 skips the row                                */
     double weight_decay;   /* this tensor's weight decay (0 disables it)               */
     int32_t rho_bits;      /* 8 or 16                                                  */
-    int32_t reserved;      /* must be 0                                                */
+    int32_t grad_dtype;    /* fo_grad_dtype_t: FO_GRAD_BF16 (0) or FO_GRAD_F32 (1)     */
 } fo_tensor_t;
 
 /* AdamW: lr > 0 finite, 0 <= beta < 1, eps > 0 (weight decay is per row). */
@@ -162,8 +175,10 @@ fo_status_t fo_dequant_state(const void *q, const uint16_t *scales, float *x, in
  * memory once per call.
  * Errors: FO_ERR_NULL, FO_ERR_MISALIGNED, FO_ERR_SIZE (numel < 0, step < 1,
  * ntensors < 0), FO_ERR_TOO_MANY_TENSORS, FO_ERR_BAD_ARG (rho_bits,
- * reserved, non-finite or out-of-range hyper-parameters), FO_ERR_ALIAS,
- * FO_ERR_CUDA. ntensors = 0 is a no-op.
+ * grad_dtype, non-finite or out-of-range hyper-parameters), FO_ERR_ALIAS,
+ * FO_ERR_CUDA. ntensors = 0 is a no-op. Rows of both correction widths and
+ * both gradient types may be mixed in one table (one launch per combination
+ * present).
  */
 fo_status_t fo_adamw_step(const fo_tensor_t *table, int32_t ntensors,
                           const fo_adamw_hparams_t *hp, int64_t step, fo_stream_t stream);

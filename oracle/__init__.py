@@ -57,6 +57,7 @@ class Tensor(ctypes.Structure):
         ("numel", ctypes.c_int64),
         ("weight_decay", ctypes.c_double),
         ("rho_bits", ctypes.c_int32),
+        ("grad_is_f32", ctypes.c_int32),
     ]
 
 
@@ -270,10 +271,12 @@ class State:
                      c(self.v_scale), self.weight_decay, self.rho_bits)
 
     def row(self, grad: np.ndarray) -> Tensor:
-        assert grad.dtype == np.uint16 and grad.size == self.numel and grad.flags.c_contiguous
+        """A table row over this state; grad is BF16 bit patterns (uint16) or float32."""
+        assert grad.dtype in (np.uint16, np.float32), grad.dtype
+        assert grad.size == self.numel and grad.flags.c_contiguous
         return Tensor(_ptr(self.theta_p), _ptr(self.rho), _ptr(self.m_q), _ptr(self.m_scale),
                       _ptr(self.v_q), _ptr(self.v_scale), _ptr(grad), self.numel,
-                      self.weight_decay, self.rho_bits)
+                      self.weight_decay, self.rho_bits, int(grad.dtype == np.float32))
 
 
 def _table(states, grads):

@@ -488,6 +488,8 @@ static int row_ok(const oracle_tensor_t *t, int opt)
 {
     if (t->numel < 0 || (t->rho_bits != 8 && t->rho_bits != 16))
         return 0;
+    if (t->grad_is_f32 != 0 && t->grad_is_f32 != 1)
+        return 0;
     if (t->numel == 0)
         return 1;
     if (!t->theta || !t->rho || !t->m_q || !t->m_scale || !t->grad)
@@ -513,7 +515,9 @@ static void step_group(const oracle_tensor_t *t, int64_t g0, int len, const step
         dequant_group(t->v_q + g0, t->v_scale[gi], len, ORACLE_VARIANCE, v);
 
     for (int i = 0; i < len; ++i) {
-        float g = oracle_bf16_to_f32(t->grad[g0 + i]);
+        /* the update is FP32: a BF16 gradient is widened, an FP32 one taken as is */
+        float g = t->grad_is_f32 ? ((const float *)t->grad)[g0 + i]
+                                 : oracle_bf16_to_f32(((const uint16_t *)t->grad)[g0 + i]);
         if (k->opt == OPT_ADAMW)
             adamw_element(&theta[i], &m[i], &v[i], g, &k->adamw,
                           decay_factor(k->lr, t->weight_decay));

@@ -32,10 +32,12 @@ typedef struct oracle_tensor {
     uint16_t *m_scale;      /* FP16 momentum group scales, ceil(numel/32)         */
     uint8_t *v_q;           /* second-moment codes, numel (AdamW only)            */
     uint16_t *v_scale;      /* FP16 second-moment group scales (AdamW only)       */
-    const uint16_t *grad;   /* BF16 gradient, numel, read only                    */
+    const void *grad;       /* gradient, numel, read only: BF16 bit patterns
+                               (uint16_t), or float when grad_is_f32 is 1      */
     int64_t numel;
     double weight_decay;
     int32_t rho_bits;
+    int32_t grad_is_f32;    /* 0: BF16 gradient; 1: FP32 gradient, used as is  */
 } oracle_tensor_t;
 
 /* Hyper-parameters are doubles (as Python floats are); the per-element

@@ -76,7 +76,7 @@ fo_status_t check_row(const fo_tensor_t &t, bool with_v)
         return FO_ERR_SIZE;
     if (t.rho_bits != 8 && t.rho_bits != 16)
         return FO_ERR_BAD_ARG;
-    if (t.reserved != 0 || !is_finite(t.weight_decay))
+    if ((t.grad_dtype != FO_GRAD_BF16 && t.grad_dtype != FO_GRAD_F32) || !is_finite(t.weight_decay))
         return FO_ERR_BAD_ARG;
     if (t.numel == 0)
         return FO_OK;
@@ -89,7 +89,7 @@ fo_status_t check_row(const fo_tensor_t &t, bool with_v)
         return FO_ERR_MISALIGNED;
     if ((reinterpret_cast<uintptr_t>(t.m_scale) & 1u) || (with_v && (reinterpret_cast<uintptr_t>(t.v_scale) & 1u)))
         return FO_ERR_MISALIGNED;
-    const int64_t n = t.numel, ng = (n + 31) / 32, gb = 2 * n;
+    const int64_t n = t.numel, ng = (n + 31) / 32, gb = (t.grad_dtype == FO_GRAD_F32 ? 4 : 2) * n;
     if (overlaps(t.grad, gb, t.theta, 2 * n) || overlaps(t.grad, gb, t.rho, n * (t.rho_bits / 8)) ||
         overlaps(t.grad, gb, t.m_q, n) || overlaps(t.grad, gb, t.m_scale, 2 * ng) ||
         (with_v && (overlaps(t.grad, gb, t.v_q, n) || overlaps(t.grad, gb, t.v_scale, 2 * ng))))
@@ -118,18 +118,21 @@ fo_status_t run_table(Opt opt, const fo_tensor_t *table, int32_t ntensors, const
             return st;
     }
 
-    // Pack rows into launches of one correction width, at most kRowsPerLaunch
-    // rows and 2^31-1 tiles each (a kernel is specialised per width).
+    // Pack rows into launches of one correction width and one gradient type,
+    // at most kRowsPerLaunch rows and 2^31-1 tiles each (a kernel is
+    // specialised per width and type).
     static thread_local fo::StepParams p;  // large: kept off the stack
     p.s = s;
-    for (const int rb : {8, 16}) {
+    for (int combo = 0; combo < 4; ++combo) {
+        const int rb = (combo & 1) ? 16 : 8;
+        const int gdt = (combo & 2) ? FO_GRAD_F32 : FO_GRAD_BF16;
         int32_t i = 0;
         while (i < ntensors) {
             int nrows = 0;
             int64_t tiles = 0;
             while (i < ntensors && nrows < fo::kRowsPerLaunch) {
                 const fo_tensor_t &t = table[i];
-                if (t.numel == 0 || t.rho_bits != rb) {
+                if (t.numel == 0 || t.rho_bits != rb || t.grad_dtype != gdt) {
                     ++i;
                     continue;
                 }
@@ -156,7 +159,7 @@ fo_status_t run_table(Opt opt, const fo_tensor_t *table, int32_t ntensors, const
                 break;
             p.nrows = nrows;
             p.total_tiles = (int32_t)tiles;
-            const fo_status_t st = cuda_status(fo::launch_step(opt, rb, p, static_cast<cudaStream_t>(stream)));
+            const fo_status_t st = cuda_status(fo::launch_step(opt, rb, gdt == FO_GRAD_F32 ? 32 : 16, p, static_cast<cudaStream_t>(stream)));
             if (st != FO_OK)
                 return st;
         }

@@ -26,7 +26,7 @@ struct StepRow {
     uint16_t *ms;
     uint8_t *vq;
     uint16_t *vs;
-    const uint16_t *grad;
+    const void *grad;   // uint16_t (BF16) or float, per the launch's gradient type
     int64_t numel;
     float coef;
     int32_t rho_bits;
@@ -65,8 +65,8 @@ struct StepParams {
 static_assert(sizeof(StepParams) <= 32764, "kernel parameter space");
 
 // Launch one fused step over p.nrows rows, all of correction width rho_bits
-// (p.total_tiles > 0).
-cudaError_t launch_step(Opt opt, int rho_bits, const StepParams &p, cudaStream_t stream);
+// and gradient width grad_bits (16: BF16, 32: FP32) (p.total_tiles > 0).
+cudaError_t launch_step(Opt opt, int rho_bits, int grad_bits, const StepParams &p, cudaStream_t stream);
 
 // Element-wise codecs.
 cudaError_t launch_split(const float *theta, uint16_t *tp, void *rho, int64_t n, int rho_bits,

@@ -32,7 +32,7 @@ constexpr int kStepMinBlocks = FO_STEP_MIN_BLOCKS;
 
 
 struct Loaded {
-    uint32_t g[8];   // 16 BF16 gradients
+    uint32_t g[16];  // 16 gradients: BF16 pairs in g[0..7], or FP32 in g[0..15]
     uint32_t t[8];   // 16 BF16 theta'
     uint32_t r[8];   // 16 rho codes (4 words for 8-bit, 8 for 16-bit)
     uint32_t m[4];   // 16 INT8 momentum codes
@@ -40,13 +40,25 @@ struct Loaded {
     uint16_t ms, vs; // the group's FP16 scales
 };
 
-template <int RB, bool WithV>
+template <int RB, bool WithV, int GB>
 __device__ __forceinline__ void load_chunk(const StepRow &row, int64_t i0, int cnt, Loaded &L)
 {
     if (cnt == kEPT) {
-        uint4 a = ld_stream(row.grad + i0), b = ld_stream(row.grad + i0 + 8);
-        L.g[0] = a.x; L.g[1] = a.y; L.g[2] = a.z; L.g[3] = a.w;
-        L.g[4] = b.x; L.g[5] = b.y; L.g[6] = b.z; L.g[7] = b.w;
+        uint4 a, b;
+        if (GB == 16) {
+            const uint16_t *gp = static_cast<const uint16_t *>(row.grad) + i0;
+            a = ld_stream(gp);
+            b = ld_stream(gp + 8);
+            L.g[0] = a.x; L.g[1] = a.y; L.g[2] = a.z; L.g[3] = a.w;
+            L.g[4] = b.x; L.g[5] = b.y; L.g[6] = b.z; L.g[7] = b.w;
+        } else {
+            const float *gp = static_cast<const float *>(row.grad) + i0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                a = ld_stream(gp + 4 * q);
+                L.g[4 * q] = a.x; L.g[4 * q + 1] = a.y; L.g[4 * q + 2] = a.z; L.g[4 * q + 3] = a.w;
+            }
+        }
         a = ld_stream(row.theta + i0);
         b = ld_stream(row.theta + i0 + 8);
         L.t[0] = a.x; L.t[1] = a.y; L.t[2] = a.z; L.t[3] = a.w;
@@ -74,7 +86,11 @@ __device__ __forceinline__ void load_chunk(const StepRow &row, int64_t i0, int c
     // ragged tail of a tensor: element-wise loads of the first cnt elements,
     // the rest read as 0 (and are masked out of the group absmax)
 #pragma unroll
-    for (int w = 0; w < 8; ++w) { L.g[w] = 0; L.t[w] = 0; L.r[w] = 0; }
+    for (int w = 0; w < 8; ++w) { L.t[w] = 0; L.r[w] = 0; }
+    constexpr int kGradWords = GB == 16 ? 8 : 16;
+#pragma unroll
+    for (int w = 0; w < kGradWords; ++w)
+        L.g[w] = 0;
 #pragma unroll
     for (int w = 0; w < 4; ++w) { L.m[w] = 0; L.v[w] = 0; }
     // the group's scales: needed by both lanes of the pair even when this lane
@@ -89,7 +105,10 @@ __device__ __forceinline__ void load_chunk(const StepRow &row, int64_t i0, int c
         if (j >= cnt)
             break;
         const int sh16 = 16 * (j & 1), sh8 = 8 * (j & 3);
-        L.g[j >> 1] |= (uint32_t)row.grad[i0 + j] << sh16;
+        if (GB == 16)
+            L.g[j >> 1] |= (uint32_t)static_cast<const uint16_t *>(row.grad)[i0 + j] << sh16;
+        else
+            L.g[j] = static_cast<const uint32_t *>(row.grad)[i0 + j];
         L.t[j >> 1] |= (uint32_t)row.theta[i0 + j] << sh16;
         if (RB == 8)
             L.r[j >> 2] |= (uint32_t)(uint8_t)static_cast<const int8_t *>(row.rho)[i0 + j] << sh8;
@@ -117,16 +136,36 @@ __device__ __forceinline__ uint32_t theta_p_bits(const uint32_t (&t)[8])
     return (J & 1) ? bf16_hi_bits(t[J >> 1]) : bf16_lo_bits(t[J >> 1]);
 }
 
+// gradient of element j as FP32 (BF16 widened exactly, or FP32 as loaded)
+template <int GB, int J>
+__device__ __forceinline__ float grad_at(const Loaded &L)
+{
+    if (GB == 16)
+        return __uint_as_float((J & 1) ? (L.g[J >> 1] & 0xFFFF0000u) : (L.g[J >> 1] << 16));
+    else
+        return __uint_as_float(L.g[J]);
+}
+
+// gradients of elements 2w and 2w+1, packed
+template <int GB, int W>
+__device__ __forceinline__ f2 grad_pair(const Loaded &L)
+{
+    if (GB == 16)
+        return pk(__uint_as_float(L.g[W] << 16), __uint_as_float(L.g[W] & 0xFFFF0000u));
+    else
+        return pk(__uint_as_float(L.g[2 * W]), __uint_as_float(L.g[2 * W + 1]));
+}
+
 // Exact path, element j: decode, update, and the new theta (FP32), the
 // companded momentum z and nr = -sqrt(v) (AdamW; 0 otherwise), with the IEEE
 // operations of the library's arithmetic contract. It serves the threads
 // whose operands fall outside the validated ranges of the packed fast path.
-template <Opt O, int RB, int J>
+template <Opt O, int RB, int GB, int J>
 __device__ __forceinline__ void element_exact(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
                                               const StepScalars &s, float coef, float cm, float cv,
                                               float &theta_out, float &z_out, float &nr_out)
 {
-    const float g = __uint_as_float(theta_p_bits<J>(L.g));
+    const float g = grad_at<GB, J>(L);
     float theta = merge_one<RB>(theta_p_bits<J>(L.t), rho_at<RB, J>(rx));
     const float zq = __fmul_rn(s8_at<J & 3>(mx[J >> 2]), cm);
     float m = phi_m_inv(zq);
@@ -157,13 +196,13 @@ __device__ __forceinline__ void element_exact(const Loaded &L, const uint32_t (&
     z_out = phi_m(m);
 }
 
-template <Opt O, int RB, int... J>
+template <Opt O, int RB, int GB, int... J>
 __device__ __forceinline__ void all_exact(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
                                           const StepScalars &s, float coef, float cm, float cv,
                                           float (&th)[kEPT], float (&z)[kEPT], float (&nr)[kEPT],
                                           std::integer_sequence<int, J...>)
 {
-    (element_exact<O, RB, J>(L, rx, mx, s, coef, cm, cv, th[J], z[J], nr[J]), ...);
+    (element_exact<O, RB, GB, J>(L, rx, mx, s, coef, cm, cv, th[J], z[J], nr[J]), ...);
 }
 
 // ---------------------------------------------------------------------------
@@ -268,13 +307,13 @@ __device__ __forceinline__ f2 phi_m_pair(f2 m)
 
 
 
-template <Opt O, int RB, int W>
+template <Opt O, int RB, int GB, int W>
 __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
                                           const StepScalars &s, const PairConsts &k,
                                           float (&th)[kEPT], float (&z)[kEPT], float (&nr)[kEPT], Guard &gd)
 {
     constexpr int j0 = 2 * W, j1 = 2 * W + 1;
-    const f2 g = pk(__uint_as_float(L.g[W] << 16), __uint_as_float(L.g[W] & 0xFFFF0000u));
+    const f2 g = grad_pair<GB, W>(L);
     float g0, g1;
     unpk(g, g0, g1);
     const f2 theta = merge_pair<RB, W>(L, rx, gd);
@@ -331,13 +370,13 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
     unpk(nrv, nr[j0], nr[j1]);
 }
 
-template <Opt O, int RB, int... W>
+template <Opt O, int RB, int GB, int... W>
 __device__ __forceinline__ void all_fast(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
                                          const StepScalars &s, const PairConsts &k,
                                          float (&th)[kEPT], float (&z)[kEPT], float (&nr)[kEPT], Guard &gd,
                                          std::integer_sequence<int, W...>)
 {
-    (pair_fast<O, RB, W>(L, rx, mx, s, k, th, z, nr, gd), ...);
+    (pair_fast<O, RB, GB, W>(L, rx, mx, s, k, th, z, nr, gd), ...);
 }
 
 __device__ __forceinline__ int chunk_count(const StepRow &row, int64_t i0)
@@ -347,7 +386,7 @@ __device__ __forceinline__ int chunk_count(const StepRow &row, int64_t i0)
 }
 
 // One thread's 16 elements of a tile, from data already loaded into L.
-template <Opt O, int RB>
+template <Opt O, int RB, int GB>
 __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalars &s, int64_t i0, int cnt,
                                             Loaded &L)
 {
@@ -386,19 +425,19 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
             gd.max_nv = -1.0f;
             gd.min_q = 1.0f;
         }
-        all_fast<O, RB>(L, rx, mx, s, k, th, z, nr, gd, std::make_integer_sequence<int, kEPT / 2>{});
+        all_fast<O, RB, GB>(L, rx, mx, s, k, th, z, nr, gd, std::make_integer_sequence<int, kEPT / 2>{});
         bad = gd.failed(O == Opt::kAdamW ? 0x1p24f : 0x1p100f);
     }
     if (bad) {
         // rare: reload (the data is unchanged) and recompute with IEEE operations
-        load_chunk<RB, WithV>(row, i0, cnt, L);
+        load_chunk<RB, WithV, GB>(row, i0, cnt, L);
 #pragma unroll
         for (int w = 0; w < 8; ++w)
             rx[w] = L.r[w] ^ (RB == 8 ? 0x80808080u : 0x80008000u);
 #pragma unroll
         for (int w = 0; w < 4; ++w)
             mx[w] = L.m[w] ^ 0x80808080u;
-        all_exact<O, RB>(L, rx, mx, s, row.coef, cm, cv, th, z, nr, std::make_integer_sequence<int, kEPT>{});
+        all_exact<O, RB, GB>(L, rx, mx, s, row.coef, cm, cv, th, z, nr, std::make_integer_sequence<int, kEPT>{});
     }
 
     // re-split theta: theta' (BF16, nearest even) and rho (see split_code;
@@ -508,8 +547,9 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
     }
 }
 
-// One launch: rows of one rho width (RB), walked tile by tile.
-template <Opt O, int RB>
+// One launch: rows of one rho width (RB) and gradient width (GB), walked
+// tile by tile.
+template <Opt O, int RB, int GB>
 __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
 fo_fused_step_kernel(const __grid_constant__ StepParams p)
 {
@@ -523,18 +563,18 @@ fo_fused_step_kernel(const __grid_constant__ StepParams p)
         const int64_t i0 = (int64_t)(tile - first) * kStepTile + (int64_t)threadIdx.x * kEPT;
         const int cnt = chunk_count(r, i0);
         Loaded L;
-        load_chunk<RB, WithV>(r, i0, cnt, L);
-        thread_step<O, RB>(r, p.s, i0, cnt, L);
+        load_chunk<RB, WithV, GB>(r, i0, cnt, L);
+        thread_step<O, RB, GB>(r, p.s, i0, cnt, L);
     }
 }
 
-template <Opt O, int RB>
+template <Opt O, int RB, int GB>
 int resident_ctas()
 {
     static int cached = 0;
     if (cached == 0) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fo_fused_step_kernel<O, RB>, kStepThreads, 0) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fo_fused_step_kernel<O, RB, GB>, kStepThreads, 0) !=
                 cudaSuccess ||
             n < 1)
             n = 1;
@@ -543,32 +583,33 @@ int resident_ctas()
     return cached;
 }
 
-template <Opt O, int RB>
+template <Opt O, int RB, int GB>
 cudaError_t launch(const StepParams &p, cudaStream_t stream)
 {
-    const long long want = (long long)sm_count() * resident_ctas<O, RB>();
+    const long long want = (long long)sm_count() * resident_ctas<O, RB, GB>();
     const int grid = (int)(want < p.total_tiles ? want : p.total_tiles);
-    fo_fused_step_kernel<O, RB><<<grid, kStepThreads, 0, stream>>>(p);
+    fo_fused_step_kernel<O, RB, GB><<<grid, kStepThreads, 0, stream>>>(p);
     count_launch();
     return cudaGetLastError();
 }
 
+template <int RB, int GB>
+cudaError_t launch_opt(Opt opt, const StepParams &p, cudaStream_t stream)
+{
+    switch (opt) {
+    case Opt::kAdamW: return launch<Opt::kAdamW, RB, GB>(p, stream);
+    case Opt::kSgd: return launch<Opt::kSgd, RB, GB>(p, stream);
+    default: return launch<Opt::kLion, RB, GB>(p, stream);
+    }
+}
+
 }  // namespace
 
-cudaError_t launch_step(Opt opt, int rho_bits, const StepParams &p, cudaStream_t stream)
+cudaError_t launch_step(Opt opt, int rho_bits, int grad_bits, const StepParams &p, cudaStream_t stream)
 {
-    if (rho_bits == 8) {
-        switch (opt) {
-        case Opt::kAdamW: return launch<Opt::kAdamW, 8>(p, stream);
-        case Opt::kSgd: return launch<Opt::kSgd, 8>(p, stream);
-        default: return launch<Opt::kLion, 8>(p, stream);
-        }
-    }
-    switch (opt) {
-    case Opt::kAdamW: return launch<Opt::kAdamW, 16>(p, stream);
-    case Opt::kSgd: return launch<Opt::kSgd, 16>(p, stream);
-    default: return launch<Opt::kLion, 16>(p, stream);
-    }
+    if (grad_bits == 32)
+        return rho_bits == 8 ? launch_opt<8, 32>(opt, p, stream) : launch_opt<16, 32>(opt, p, stream);
+    return rho_bits == 8 ? launch_opt<8, 16>(opt, p, stream) : launch_opt<16, 16>(opt, p, stream);
 }
 
 }  // namespace fo

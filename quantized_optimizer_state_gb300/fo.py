@@ -14,6 +14,8 @@ from typing import Iterable, List, Optional, Sequence
 from . import build as _build
 
 GROUP = 32
+GRAD_BF16 = 0   # fo_grad_dtype_t
+GRAD_F32 = 1
 FO_STATE_MOMENTUM = 0
 FO_STATE_VARIANCE = 1
 FO_MAX_TENSORS = 1 << 20
@@ -41,7 +43,7 @@ class FoTensor(ctypes.Structure):
         ("numel", ctypes.c_int64),
         ("weight_decay", ctypes.c_double),
         ("rho_bits", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("grad_dtype", ctypes.c_int32),
     ]
 
 
@@ -167,10 +169,20 @@ class Table:
         return ctypes.addressof(self.rows)
 
 
+def _grad_dtype(grad, grad_dtype: Optional[int]) -> int:
+    """FP32 for a float32 tensor, else BF16 (bfloat16 or int16 bit patterns);
+    an explicit grad_dtype wins (needed for raw pointers)."""
+    if grad_dtype is not None:
+        return int(grad_dtype)
+    dt = getattr(grad, "dtype", None)
+    return GRAD_F32 if dt is not None and str(dt) == "torch.float32" else GRAD_BF16
+
+
 def row(theta, rho, m_q, m_scale, grad, v_q=None, v_scale=None, weight_decay: float = 0.0,
-        rho_bits: int = 8, numel: Optional[int] = None) -> FoTensor:
+        rho_bits: int = 8, numel: Optional[int] = None, grad_dtype: Optional[int] = None) -> FoTensor:
     return FoTensor(_ptr(theta), _ptr(rho), _ptr(m_q), _ptr(m_scale), _ptr(v_q), _ptr(v_scale),
-                    _ptr(grad), _numel(theta, numel), float(weight_decay), int(rho_bits), 0)
+                    _ptr(grad), _numel(theta, numel), float(weight_decay), int(rho_bits),
+                    _grad_dtype(grad, grad_dtype))
 
 
 def fo_adamw_step(table: Table, lr: float, beta1: float, beta2: float, eps: float, step: int,

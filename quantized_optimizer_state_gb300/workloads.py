@@ -282,6 +282,12 @@ def init_weight_device(spec: ParamSpec, tensor_index: int, device, seed: int = W
 def grad_bf16_device(kind: str, scale: float, n: int, tensor_index: int, step: int, device):
     """BF16 gradient of one tensor drawn on the device."""
     import torch
+    return grad_fp32_device(kind, scale, n, tensor_index, step, device).to(torch.bfloat16)
+
+
+def grad_fp32_device(kind: str, scale: float, n: int, tensor_index: int, step: int, device):
+    """FP32 gradient of one tensor drawn on the device (the BF16 one before rounding)."""
+    import torch
     g = _torch_gen(device, GRAD_SEED_BASE + step, tensor_index)
     if kind == "normal":
         x = torch.randn(n, generator=g, device=device, dtype=torch.float32).mul_(scale)
@@ -297,4 +303,4 @@ def grad_bf16_device(kind: str, scale: float, n: int, tensor_index: int, step: i
         x = torch.where((u >= 0.01) & (u < 0.011), torch.zeros_like(x), x)
     else:
         raise KeyError(kind)
-    return x.to(torch.bfloat16)
+    return x

@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_struct_layout_matches_header():
-    # 7 pointers, int64 numel, double weight_decay, int32 rho_bits, int32 reserved
+    # 7 pointers, int64 numel, double weight_decay, int32 rho_bits, int32 grad_dtype
     assert ctypes.sizeof(fo.FoTensor) == 80
     assert fo.FoTensor.numel.offset == 56 and fo.FoTensor.weight_decay.offset == 64
     assert ctypes.sizeof(fo.AdamWHparams) == 32
@@ -63,7 +63,7 @@ def _table(**over):
     A = 1 << 24
     base = dict(theta=A, rho=A + (1 << 20), m_q=A + (2 << 20), m_scale=A + (3 << 20),
                 v_q=A + (4 << 20), v_scale=A + (5 << 20), grad=A + (6 << 20), numel=100,
-                weight_decay=0.01, rho_bits=8, reserved=0)
+                weight_decay=0.01, rho_bits=8, grad_dtype=0)
     base.update(over)
     return fo.FoTensor(**base)
 
@@ -82,11 +82,15 @@ def test_step_argument_errors():
     assert _adamw([_table(theta=None)]) == 1
     assert _adamw([_table(v_q=None)]) == 1                         # AdamW needs v
     assert _adamw([_table(rho_bits=4)]) == 4
-    assert _adamw([_table(reserved=1)]) == 4
+    assert _adamw([_table(grad_dtype=2)]) == 4                     # not BF16 (0) or FP32 (1)
+    assert _adamw([_table(grad_dtype=-1)]) == 4
     assert _adamw([_table(weight_decay=float("nan"))]) == 4
     assert _adamw([_table(grad=(1 << 24) + (6 << 20) + 8)]) == 2   # misaligned grad
     assert _adamw([_table(m_scale=(1 << 24) + (3 << 20) + 1)]) == 2
     assert _adamw([_table(grad=(1 << 24) + 64)]) == 7              # grad overlaps theta'
+    # an FP32 gradient spans 4 bytes an element: 100 of them from 304 bytes
+    # below rho reach into it (100 BF16 ones would not)
+    assert _adamw([_table(grad=(1 << 24) + (1 << 20) - 304, grad_dtype=1)]) == 7
     assert _adamw([_table()], lr=float("inf")) == 4
     assert _adamw([_table()], beta1=1.0) == 4
     assert _adamw([_table()], eps=0.0) == 4

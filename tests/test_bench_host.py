@@ -81,3 +81,16 @@ def test_reference_arm_line(monkeypatch, capsys):
     assert line["impl"] == "reference" and line["unit"] == "params/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["config"]["params"] == 8_030_261_248
+
+
+def test_algorithmic_bytes_per_param():
+    """Each state byte read and written once, the gradient read once: AdamW with
+    8-bit rho moves 2+2+1+1+1 + 2*2/32 read and 2+1+1+1 + 2*2/32 written."""
+    from quantized_optimizer_state_gb300 import workloads as wl
+    adamw = wl.workload("flat_1m")
+    lion = wl.workload("llama31_8b_lion")
+    assert bench._algo_bytes(adamw, 8) == 12.25
+    assert bench._algo_bytes(adamw, 16) == 14.25
+    assert bench._algo_bytes(adamw, 8, "f32") == 14.25
+    assert bench._algo_bytes(lion, 8) == 2 + 2 * (2 + 1 + 1 + 2 / 32)
+    assert bench._algo_bytes(lion, 16, "f32") == 4 + 2 * (2 + 2 + 1 + 2 / 32)

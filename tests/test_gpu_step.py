@@ -206,10 +206,15 @@ def _chunk_state(d: fo.CompressedTensor, lo: int, hi: int) -> oracle.State:
                         d.weight_decay, d.rho_bits)
 
 
+def _grad_host(g: torch.Tensor) -> np.ndarray:
+    """A device gradient slice as the oracle takes it: BF16 patterns or float32."""
+    return to_host(g) if g.dtype == torch.float32 else to_host(g.view(torch.int16))
+
+
 def _sampled_parity(opt, dev, grads_dev, samples, t, hp):
     """Run one GPU step over all rows; check sampled chunks against the oracle
     run on the same chunks' pre-step state (groups are independent)."""
-    pre = [( i, lo, hi, _chunk_state(dev[i], lo, hi), to_host(grads_dev[i][lo:hi].view(torch.int16)))
+    pre = [(i, lo, hi, _chunk_state(dev[i], lo, hi), _grad_host(grads_dev[i][lo:hi]))
            for i, lo, hi in samples]
     _gpu_step(opt, dev, grads_dev, t, hp)
     for i, lo, hi, st, g in pre:
@@ -231,8 +236,9 @@ def _samples_of(sizes, per_row=1 << 16, rows=None):
     return out
 
 
-def _device_workload(w, dtype_rho=8):
+def _device_workload(w, grad_fp32=False):
     dev, grads = [], []
+    gen = wl.grad_fp32_device if grad_fp32 else wl.grad_bf16_device
     for i, p in enumerate(w.params):
         d = fo.CompressedTensor(p.numel, "cuda", w.rho_bits, w.optimizer == "adamw",
                                 w.hparams["weight_decay"])
@@ -240,7 +246,7 @@ def _device_workload(w, dtype_rho=8):
         d.init_from(theta)
         del theta
         dev.append(d)
-        grads.append(wl.grad_bf16_device(w.grad, w.grad_scale, p.numel, i, 1, "cuda"))
+        grads.append(gen(w.grad, w.grad_scale, p.numel, i, 1, "cuda"))
     torch.cuda.synchronize()
     return dev, grads
 
