@@ -83,8 +83,13 @@ typedef enum fo_status {
 
 /* Kind of optimizer state coded by fo_quant_state / fo_dequant_state. */
 typedef enum fo_state_kind {
-    FO_STATE_MOMENTUM = 0, /* INT8 codes (int8_t), phi_m companding  */
-    FO_STATE_VARIANCE = 1  /* UINT8 codes (uint8_t), phi_v companding */
+    FO_STATE_MOMENTUM = 0,        /* INT8 codes (int8_t), phi_m companding   */
+    FO_STATE_VARIANCE = 1,        /* UINT8 codes (uint8_t), phi_v companding */
+    /* The same group quantization with phi the identity: the plain linear
+     * quantizer that section "实验结果分析" (Fig. 4, Fig. 5) compares the
+     * companded codecs against. For quality studies; the step never uses it. */
+    FO_STATE_MOMENTUM_LINEAR = 2, /* INT8 codes of m itself                  */
+    FO_STATE_VARIANCE_LINEAR = 3  /* UINT8 codes of v itself                 */
 } fo_state_kind_t;
 
 #define FO_GROUP 32               /* elements per quantization group            */
@@ -151,8 +156,8 @@ fo_status_t fo_merge(const uint16_t *theta_bf16, const void *rho, float *theta_f
 /*
  * fo_quant_state -- companded group quantization, section
  * "带压缩扩展的优化器状态量化" (Algorithm 2 for m, Algorithm 3 for v):
- * x[n] (FP32; v must be >= 0) -> codes q[n] (int8_t for FO_STATE_MOMENTUM,
- * uint8_t for FO_STATE_VARIANCE) and scales[ceil(n/32)] (FP16).
+ * x[n] (FP32; v must be >= 0) -> codes q[n] (int8_t for the momentum kinds,
+ * uint8_t for the variance kinds) and scales[ceil(n/32)] (FP16).
  * Errors: FO_ERR_NULL, FO_ERR_MISALIGNED, FO_ERR_SIZE, FO_ERR_BAD_ARG (kind),
  * FO_ERR_CUDA. n = 0 is a no-op.
  */

@@ -24,6 +24,8 @@ _lib = None
 
 MOMENTUM = 0
 VARIANCE = 1
+MOMENTUM_LINEAR = 2   # group quantization without companding (Fig. 4's comparison)
+VARIANCE_LINEAR = 3
 GROUP = 32
 
 # -ffp-contract=off: no implicit fused multiply-add (gcc contracts by default on
@@ -218,16 +220,22 @@ def merge(theta_p: np.ndarray, rho: np.ndarray, rho_bits: int = 8) -> np.ndarray
     return out
 
 
+def _code_dtype(kind: int):
+    if kind not in (MOMENTUM, VARIANCE, MOMENTUM_LINEAR, VARIANCE_LINEAR):
+        raise ValueError(f"unknown state kind {kind}")
+    return np.int8 if kind in (MOMENTUM, MOMENTUM_LINEAR) else np.uint8
+
+
 def quant_state(x: np.ndarray, kind: int):
     x = np.ascontiguousarray(x, dtype=np.float32)
-    q = np.empty(x.shape, np.int8 if kind == MOMENTUM else np.uint8)
+    q = np.empty(x.shape, _code_dtype(kind))
     scales = np.empty((x.size + GROUP - 1) // GROUP, np.uint16)
     lib().oracle_quant_state(_ptr(x), _ptr(q), _ptr(scales), x.size, kind)
     return q, scales
 
 
 def dequant_state(q: np.ndarray, scales: np.ndarray, kind: int) -> np.ndarray:
-    q = np.ascontiguousarray(q, dtype=np.int8 if kind == MOMENTUM else np.uint8)
+    q = np.ascontiguousarray(q, dtype=_code_dtype(kind))
     scales = np.ascontiguousarray(scales, dtype=np.uint16)
     out = np.empty(q.shape, np.float32)
     lib().oracle_dequant_state(_ptr(q), _ptr(scales), _ptr(out), q.size, kind)

@@ -272,21 +272,44 @@ void oracle_merge(const uint16_t *theta_p, const void *rho, float *theta, int64_
  *    [0, 255]; a group whose scale is 0 stores all codes 0;
  *  - groups are 32 consecutive elements of one tensor; the last group of a
  *    tensor holds the remaining numel mod 32 elements.
+ * The linear kinds are the same steps with phi the identity (Fig. 4's plain
+ * group-wise linear quantization).
  */
+
+/* phi of a state kind (identity for the linear kinds) */
+static float compand(float x, int kind)
+{
+    switch (kind) {
+    case ORACLE_MOMENTUM: return oracle_phi_m(x);
+    case ORACLE_VARIANCE: return oracle_phi_v(x);
+    default: return x;
+    }
+}
+
+static float expand(float z, int kind)
+{
+    switch (kind) {
+    case ORACLE_MOMENTUM: return oracle_phi_m_inv(z);
+    case ORACLE_VARIANCE: return oracle_phi_v_inv(z);
+    default: return z;
+    }
+}
+
+static int kind_signed(int kind) { return kind == ORACLE_MOMENTUM || kind == ORACLE_MOMENTUM_LINEAR; }
 static void quant_group(const float *x, int len, int kind, void *q, uint16_t *scale)
 {
     float c[ORACLE_GROUP];
     float a = 0.0f;
     for (int i = 0; i < len; ++i) {
-        c[i] = kind == ORACLE_MOMENTUM ? oracle_phi_m(x[i]) : oracle_phi_v(x[i]);
+        c[i] = compand(x[i], kind);
         if (fabsf(c[i]) > a)
             a = fabsf(c[i]);
     }
     uint16_t s = oracle_fp16_rne(fminf(a, 65504.0f));
     float sf = oracle_fp16_to_f32(s);
     *scale = s;
-    const float levels = kind == ORACLE_MOMENTUM ? 127.0f : 255.0f;
-    const float lo = kind == ORACLE_MOMENTUM ? -127.0f : 0.0f;
+    const float levels = kind_signed(kind) ? 127.0f : 255.0f;
+    const float lo = kind_signed(kind) ? -127.0f : 0.0f;
     float inv = sf == 0.0f ? 0.0f : levels / sf;
     for (int i = 0; i < len; ++i) {
         float code = 0.0f;
@@ -297,7 +320,7 @@ static void quant_group(const float *x, int len, int kind, void *q, uint16_t *sc
             if (code < lo)
                 code = lo;
         }
-        if (kind == ORACLE_MOMENTUM)
+        if (kind_signed(kind))
             ((int8_t *)q)[i] = (int8_t)code;
         else
             ((uint8_t *)q)[i] = (uint8_t)code;
@@ -307,18 +330,10 @@ static void quant_group(const float *x, int len, int kind, void *q, uint16_t *sc
 static void dequant_group(const void *q, uint16_t scale, int len, int kind, float *x)
 {
     float sf = oracle_fp16_to_f32(scale);
-    if (kind == ORACLE_MOMENTUM) {
-        float step = sf / 127.0f;
-        for (int i = 0; i < len; ++i) {
-            float zhat = (float)((const int8_t *)q)[i] * step;
-            x[i] = oracle_phi_m_inv(zhat);
-        }
-    } else {
-        float step = sf / 255.0f;
-        for (int i = 0; i < len; ++i) {
-            float rhat = (float)((const uint8_t *)q)[i] * step;
-            x[i] = oracle_phi_v_inv(rhat);
-        }
+    float step = sf / (kind_signed(kind) ? 127.0f : 255.0f);
+    for (int i = 0; i < len; ++i) {
+        float code = kind_signed(kind) ? (float)((const int8_t *)q)[i] : (float)((const uint8_t *)q)[i];
+        x[i] = expand(code * step, kind);
     }
 }
 

@@ -22,7 +22,10 @@ extern "C" {
 
 #define ORACLE_GROUP 32 /* quantization group size G ("companded state quantization" section) */
 
-enum { ORACLE_MOMENTUM = 0, ORACLE_VARIANCE = 1 };
+/* state kinds: the companded codecs of the method, and the same group
+ * quantization without companding (the ablation the page compares against in
+ * Fig. 4 and Fig. 5): odd kinds are unsigned (second moment), even signed */
+enum { ORACLE_MOMENTUM = 0, ORACLE_VARIANCE = 1, ORACLE_MOMENTUM_LINEAR = 2, ORACLE_VARIANCE_LINEAR = 3 };
 
 /* One row of the parameter table: the compressed state of one tensor. */
 typedef struct oracle_tensor {
@@ -71,7 +74,7 @@ float oracle_phi_v_inv(float z);
 void oracle_split(const float *theta, uint16_t *theta_p, void *rho, int64_t n, int rho_bits);
 void oracle_merge(const uint16_t *theta_p, const void *rho, float *theta, int64_t n, int rho_bits);
 
-/* group quantization of one state tensor (kind: ORACLE_MOMENTUM or ORACLE_VARIANCE) */
+/* group quantization of one state tensor (kind: one of the ORACLE_* state kinds) */
 void oracle_quant_state(const float *x, void *q, uint16_t *scales, int64_t n, int kind);
 void oracle_dequant_state(const void *q, const uint16_t *scales, float *x, int64_t n, int kind);
 

@@ -180,6 +180,12 @@ float wd_coef(double, double wd) { return (float)wd; }
 
 bool beta_ok(double b) { return is_finite(b) && b >= 0.0 && b < 1.0; }
 
+bool kind_ok(fo_state_kind_t kind)
+{
+    return kind == FO_STATE_MOMENTUM || kind == FO_STATE_VARIANCE || kind == FO_STATE_MOMENTUM_LINEAR ||
+           kind == FO_STATE_VARIANCE_LINEAR;
+}
+
 fo_status_t check_codec(const void *a, const void *b, const void *c, int64_t n)
 {
     if (n < 0)
@@ -227,7 +233,7 @@ fo_status_t fo_quant_state(const float *x, void *q, uint16_t *scales, int64_t n,
     fo_status_t st = check_codec(x, q, scales, n);
     if (st != FO_OK || n == 0)
         return st;
-    if (kind != FO_STATE_MOMENTUM && kind != FO_STATE_VARIANCE)
+    if (!kind_ok(kind))
         return FO_ERR_BAD_ARG;
     if (!aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(scales) & 1u))
         return FO_ERR_MISALIGNED;
@@ -240,7 +246,7 @@ fo_status_t fo_dequant_state(const void *q, const uint16_t *scales, float *x, in
     fo_status_t st = check_codec(q, scales, x, n);
     if (st != FO_OK || n == 0)
         return st;
-    if (kind != FO_STATE_MOMENTUM && kind != FO_STATE_VARIANCE)
+    if (!kind_ok(kind))
         return FO_ERR_BAD_ARG;
     if (!aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(scales) & 1u))
         return FO_ERR_MISALIGNED;

@@ -154,7 +154,32 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const uint16_t *__restr
     }
 }
 
-// kind 0: momentum (INT8, phi_m); kind 1: second moment (UINT8, phi_v).
+// kind 0: momentum (INT8, phi_m); kind 1: second moment (UINT8, phi_v);
+// kinds 2 and 3: the same group quantization without companding (phi the
+// identity), the linear quantizer the page compares against in Fig. 4.
+template <int Kind>
+struct KindTraits {
+    static constexpr bool kSigned = (Kind & 1) == 0;
+    static constexpr bool kCompanded = Kind < 2;
+    static constexpr float kLevels = kSigned ? 127.0f : 255.0f;
+};
+
+template <int Kind>
+__device__ __forceinline__ float compand(float x)
+{
+    if (!KindTraits<Kind>::kCompanded)
+        return x;
+    return KindTraits<Kind>::kSigned ? phi_m(x) : __fsqrt_rn(x);
+}
+
+template <int Kind>
+__device__ __forceinline__ float expand(float d)
+{
+    if (!KindTraits<Kind>::kCompanded)
+        return d;
+    return KindTraits<Kind>::kSigned ? phi_m_inv(d) : __fmul_rn(d, d);
+}
+
 template <int Kind>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const float *__restrict__ xin, void *__restrict__ q,
                                                          uint16_t *__restrict__ scales, int64_t n, Chunking ck)
@@ -179,17 +204,17 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const float *__restrict
         float a = 0.0f;
 #pragma unroll
         for (int j = 0; j < kEPT; ++j) {
-            y[j] = Kind == 0 ? phi_m(y[j]) : __fsqrt_rn(y[j]);
+            y[j] = compand<Kind>(y[j]);
             if (j < cnt)
                 a = fmaxf(a, fabsf(y[j]));
         }
         a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
         const uint16_t s = scale_of(a);
-        const float mult = code_multiplier(scale_value(s), Kind == 0 ? 127.0f : 255.0f);
+        const float mult = code_multiplier(scale_value(s), KindTraits<Kind>::kLevels);
         uint32_t cw[kEPT];
 #pragma unroll
         for (int j = 0; j < kEPT; ++j)
-            cw[j] = Kind == 0 ? m_code(y[j], mult) : v_code(y[j], mult);
+            cw[j] = KindTraits<Kind>::kSigned ? m_code(y[j], mult) : v_code(y[j], mult);
         if (cnt == kEPT) {
             uint32_t o[4];
 #pragma unroll
@@ -228,13 +253,13 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const void *__restric
                 if (j < cnt)
                     w[j >> 2] |= (uint32_t)static_cast<const uint8_t *>(q)[i0 + j] << (8 * (j & 3));
         }
-        const float step = __fdiv_rn(scale_value(scales[i0 >> 5]), Kind == 0 ? 127.0f : 255.0f);
+        const float step = __fdiv_rn(scale_value(scales[i0 >> 5]), KindTraits<Kind>::kLevels);
         float x[kEPT];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const uint32_t wx = Kind == 0 ? (w[k] ^ 0x80808080u) : w[k];
+            const uint32_t wx = KindTraits<Kind>::kSigned ? (w[k] ^ 0x80808080u) : w[k];
             float c0, c1, c2, c3;
-            if (Kind == 0) {
+            if (KindTraits<Kind>::kSigned) {
                 c0 = s8_at<0>(wx); c1 = s8_at<1>(wx); c2 = s8_at<2>(wx); c3 = s8_at<3>(wx);
             } else {
                 c0 = u8_at<0>(wx); c1 = u8_at<1>(wx); c2 = u8_at<2>(wx); c3 = u8_at<3>(wx);
@@ -243,7 +268,7 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const void *__restric
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float d = __fmul_rn(cc[e], step);
-                x[4 * k + e] = Kind == 0 ? phi_m_inv(d) : __fmul_rn(d, d);
+                x[4 * k + e] = expand<Kind>(d);
             }
         }
         if (cnt == kEPT) {
@@ -294,10 +319,12 @@ cudaError_t launch_quant(const float *x, void *q, uint16_t *scales, int64_t n, i
 {
     int grid = 0;
     const Chunking ck = plan(n, &grid);
-    if (kind == 0)
-        quant_kernel<0><<<grid, kThreads, 0, stream>>>(x, q, scales, n, ck);
-    else
-        quant_kernel<1><<<grid, kThreads, 0, stream>>>(x, q, scales, n, ck);
+    switch (kind) {
+    case 0: quant_kernel<0><<<grid, kThreads, 0, stream>>>(x, q, scales, n, ck); break;
+    case 1: quant_kernel<1><<<grid, kThreads, 0, stream>>>(x, q, scales, n, ck); break;
+    case 2: quant_kernel<2><<<grid, kThreads, 0, stream>>>(x, q, scales, n, ck); break;
+    default: quant_kernel<3><<<grid, kThreads, 0, stream>>>(x, q, scales, n, ck); break;
+    }
     count_launch();
     return cudaGetLastError();
 }
@@ -307,10 +334,12 @@ cudaError_t launch_dequant(const void *q, const uint16_t *scales, float *x, int6
 {
     int grid = 0;
     const Chunking ck = plan(n, &grid);
-    if (kind == 0)
-        dequant_kernel<0><<<grid, kThreads, 0, stream>>>(q, scales, x, n, ck);
-    else
-        dequant_kernel<1><<<grid, kThreads, 0, stream>>>(q, scales, x, n, ck);
+    switch (kind) {
+    case 0: dequant_kernel<0><<<grid, kThreads, 0, stream>>>(q, scales, x, n, ck); break;
+    case 1: dequant_kernel<1><<<grid, kThreads, 0, stream>>>(q, scales, x, n, ck); break;
+    case 2: dequant_kernel<2><<<grid, kThreads, 0, stream>>>(q, scales, x, n, ck); break;
+    default: dequant_kernel<3><<<grid, kThreads, 0, stream>>>(q, scales, x, n, ck); break;
+    }
     count_launch();
     return cudaGetLastError();
 }

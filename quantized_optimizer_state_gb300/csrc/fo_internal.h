@@ -13,7 +13,14 @@ constexpr int kElemsPerThread = 16;  // one thread holds half a group
 #define FO_STEP_THREADS 256
 #endif
 constexpr int kStepThreads = FO_STEP_THREADS;
-constexpr int kStepTile = kStepThreads * kElemsPerThread;  // 4096 elements per tile
+// chunks of kStepThreads * kElemsPerThread elements a CTA steps per tile (the
+// row lookup and per-row constants are shared by a tile's chunks)
+#ifndef FO_STEP_CHUNKS
+#define FO_STEP_CHUNKS 2
+#endif
+constexpr int kStepChunks = FO_STEP_CHUNKS;
+constexpr int kStepChunk = kStepThreads * kElemsPerThread;  // 4096 elements
+constexpr int kStepTile = kStepChunk * kStepChunks;
 
 enum class Opt : int { kAdamW = 0, kSgd = 1, kLion = 2 };
 

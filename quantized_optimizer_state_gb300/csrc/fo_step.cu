@@ -560,11 +560,15 @@ fo_fused_step_kernel(const __grid_constant__ StepParams p)
             ++row;
         const int first = row == 0 ? 0 : p.tile_end[row - 1];
         const StepRow &r = p.rows[row];
-        const int64_t i0 = (int64_t)(tile - first) * kStepTile + (int64_t)threadIdx.x * kEPT;
-        const int cnt = chunk_count(r, i0);
-        Loaded L;
-        load_chunk<RB, WithV, GB>(r, i0, cnt, L);
-        thread_step<O, RB, GB>(r, p.s, i0, cnt, L);
+        const int64_t t0 = (int64_t)(tile - first) * kStepTile + (int64_t)threadIdx.x * kEPT;
+#pragma unroll 1
+        for (int c = 0; c < kStepChunks; ++c) {
+            const int64_t i0 = t0 + (int64_t)c * kStepChunk;
+            const int cnt = chunk_count(r, i0);
+            Loaded L;
+            load_chunk<RB, WithV, GB>(r, i0, cnt, L);
+            thread_step<O, RB, GB>(r, p.s, i0, cnt, L);
+        }
     }
 }
 

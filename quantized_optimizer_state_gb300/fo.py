@@ -18,6 +18,8 @@ GRAD_BF16 = 0   # fo_grad_dtype_t
 GRAD_F32 = 1
 FO_STATE_MOMENTUM = 0
 FO_STATE_VARIANCE = 1
+FO_STATE_MOMENTUM_LINEAR = 2   # group quantization without companding (quality studies)
+FO_STATE_VARIANCE_LINEAR = 3
 FO_MAX_TENSORS = 1 << 20
 
 STATUS = {0: "FO_OK", 1: "FO_ERR_NULL", 2: "FO_ERR_MISALIGNED", 3: "FO_ERR_SIZE",

@@ -104,17 +104,24 @@ def _state_inputs(kind, n, seed):
         x[64:96] = (rng.standard_normal(32) * 1e-9).astype(np.float32)  # subnormal-FP16 scale
         x[96:128] = (rng.standard_normal(32) * 1e3).astype(np.float32)  # large values
         x[128:160] = -1e-30                                    # scale rounds to 0
-    if kind == fo.FO_STATE_VARIANCE:
+    if kind in (fo.FO_STATE_VARIANCE, fo.FO_STATE_VARIANCE_LINEAR):
         x = np.abs(x) * np.abs(x)
         x = x.astype(np.float32)
     return x
 
 
-@pytest.mark.parametrize("kind", [fo.FO_STATE_MOMENTUM, fo.FO_STATE_VARIANCE])
+KINDS = [fo.FO_STATE_MOMENTUM, fo.FO_STATE_VARIANCE, fo.FO_STATE_MOMENTUM_LINEAR, fo.FO_STATE_VARIANCE_LINEAR]
+
+
+def _signed(kind):
+    return kind in (fo.FO_STATE_MOMENTUM, fo.FO_STATE_MOMENTUM_LINEAR)
+
+
+@pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("n", RAGGED + [1 << 22])
 def test_quant_matches_oracle(kind, n):
     x = _state_inputs(kind, n, n + kind)
-    q = torch.empty(n, dtype=torch.int8 if kind == 0 else torch.uint8, device="cuda")
+    q = torch.empty(n, dtype=torch.int8 if _signed(kind) else torch.uint8, device="cuda")
     s = torch.empty((n + 31) // 32, dtype=torch.int16, device="cuda")
     fo.fo_quant_state(to_dev(x), q, s, kind)
     q_ref, s_ref = oracle.quant_state(x, kind)
@@ -122,17 +129,18 @@ def test_quant_matches_oracle(kind, n):
     assert_scales(to_host(s), s_ref, "scales")
 
 
-@pytest.mark.parametrize("kind", [fo.FO_STATE_MOMENTUM, fo.FO_STATE_VARIANCE])
+@pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("n", [1, 33, 1000, (1 << 20) + 7])
 def test_dequant_matches_oracle(kind, n):
     rng = np.random.default_rng(n)
-    if kind == 0:
+    if _signed(kind):
         q = rng.integers(-127, 128, n).astype(np.int8)
     else:
         q = rng.integers(0, 256, n).astype(np.uint8)
     ng = (n + 31) // 32
-    # every finite non-negative FP16 scale below 2 for m (|z| < 2); any finite for v
-    top = 0x4000 if kind == 0 else 0x7BFF
+    # every finite non-negative FP16 scale below 2 for companded m (|z| < 2);
+    # any finite scale otherwise
+    top = 0x4000 if kind == fo.FO_STATE_MOMENTUM else 0x7BFF
     s = rng.integers(0, top + 1, ng).astype(np.uint16)
     out = torch.empty(n, device="cuda")
     fo.fo_dequant_state(to_dev(q), to_dev(s), out, kind)

@@ -4,12 +4,13 @@ What the FlashOptim page fixes (section "带压缩扩展的优化器状态量化
 companded optimizer-state quantization; Algorithms 2-3, Fig. 4):
   * phi_m(x) = 2x/(1+|x|), phi_m^-1(z) = z/(2-|z|); phi_v(x) = sqrt(x), phi_v^-1(z) = z^2;
   * groups of G = 32, one FP16 scale per group; momentum INT8, variance UINT8;
-  * companding lowers the quantization error, a little for m and a lot for v.
+  * companding lowers the quantization error, a little for m and a lot for v
+    (Fig. 4, against plain group-wise linear quantization: the linear kinds).
 """
 import numpy as np
 import pytest
 
-M, V = 0, 1
+M, V, ML, VL = 0, 1, 2, 3   # companded m, v; linear (no companding) m, v
 ULP = 2.0 ** -23
 
 
@@ -141,10 +142,11 @@ def test_companding_reduces_error_more_for_variance(orc):
     v = (1e-3 * g * g).astype(np.float32)
 
     def linear(x, levels, signed):
+        # the same storage format: one FP16 scale per group of 32
         xg = x.astype(np.float64).reshape(-1, 32)
-        s = np.abs(xg).max(1, keepdims=True)
-        s[s == 0] = 1
-        q = np.clip(np.rint(xg / s * levels), -levels if signed else 0, levels)
+        s = _fp16_values(np.minimum(np.abs(xg).max(1, keepdims=True), 65504.0))
+        with np.errstate(divide="ignore", invalid="ignore"):
+            q = np.where(s > 0, np.clip(np.rint(xg / s * levels), -levels if signed else 0, levels), 0)
         return (q * s / levels).ravel()
 
     qm, sm = orc.quant_state(m, M)
@@ -155,3 +157,57 @@ def test_companding_reduces_error_more_for_variance(orc):
     e_v_lin = _nmse(v.astype(np.float64), linear(v, 255, False))
     assert e_m_comp <= e_m_lin * 1.05
     assert e_v_comp < e_v_lin / 4
+    # the oracle's linear kinds are the same quantizer (FP16 scales, FP32 steps)
+    for x, kind, ref in ((m, ML, e_m_lin), (v, VL, e_v_lin)):
+        q, s = orc.quant_state(x, kind)
+        e = _nmse(x.astype(np.float64), orc.dequant_state(q, s, kind).astype(np.float64))
+        assert abs(e - ref) <= 0.01 * ref
+
+
+def _fp16_values(x):
+    return np.asarray(x, np.float64).astype(np.float16).astype(np.float64)
+
+
+@pytest.mark.parametrize("kind,levels", [(ML, 127), (VL, 255)])
+def test_linear_codes_on_an_exact_grid(orc, kind, levels):
+    """Values k*s/L with s an FP16 value and the group maximum equal to s:
+    the linear codec returns k itself, and decodes to k * RN(s/L)."""
+    s = 0.375
+    ks = np.arange(-127, 128) if levels == 127 else np.arange(0, 256)
+    ks = np.concatenate([ks, np.full((-len(ks)) % 32, ks[-1])])   # whole groups, max = s
+    x = (ks * (s / levels)).astype(np.float32)
+    x[31::32] = np.float32(s)
+    q, sc = orc.quant_state(x, kind)
+    assert np.all(orc.fp16_to_f32_n(sc) == s)
+    want = ks.copy()
+    want[31::32] = levels
+    assert np.array_equal(q.astype(np.int64), want)
+    d = orc.dequant_state(q, sc, kind)
+    assert np.array_equal(d, (q.astype(np.float32) * np.float32(np.float32(s) / np.float32(levels))))
+
+
+@pytest.mark.parametrize("kind,levels,signed", [(ML, 127, True), (VL, 255, False)])
+def test_linear_codec_matches_its_float64_definition(orc, kind, levels, signed):
+    """scale = FP16(max |x|); code = clamp(rint(x * L / scale)); the FP32 steps of
+    the oracle differ from the float64 definition only at rounding ties."""
+    rng = np.random.default_rng(31)
+    g = rng.standard_t(3, 32 * 4096) * 10.0 ** rng.uniform(-8, 2, 32 * 4096).repeat(1)
+    x = (g if signed else g * g).astype(np.float32)
+    q, sc = orc.quant_state(x, kind)
+    xg = x.astype(np.float64).reshape(-1, 32)
+    s64 = _fp16_values(np.minimum(np.abs(xg).max(1), 65504.0))   # the scale is capped at FP16's max
+    assert np.array_equal(orc.fp16_to_f32_n(sc).astype(np.float64), s64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        c64 = np.where(s64[:, None] > 0, np.rint(xg * (levels / s64[:, None])), 0)
+    c64 = np.clip(c64, -levels if signed else 0, levels).ravel()
+    d = q.astype(np.int64) - c64.astype(np.int64)
+    assert np.abs(d).max() <= 1 and np.count_nonzero(d) <= 1e-4 * x.size
+    # and where the scale is a normal FP16 value below the cap, every element
+    # lies within half a step of its decoded value (capped groups saturate,
+    # subnormal scales may fall below the group maximum)
+    xh = orc.dequant_state(q, sc, kind).astype(np.float64).reshape(-1, 32)
+    step = s64[:, None] / levels
+    honest = (s64 >= 2.0 ** -14) & (np.abs(xg).max(1) <= 65504.0)
+    assert honest.mean() > 0.5
+    ok = np.abs(xh - xg) <= 0.5 * step * (1 + 2.0 ** -10) + np.abs(xg) * 2.0 ** -22
+    assert np.all(ok[honest])
