@@ -52,12 +52,26 @@ def parse_args(argv=None):
     p.add_argument("--rho-bits", type=int, default=8, choices=(8, 16))
     p.add_argument("--grad-dtype", default="bf16", choices=tuple(GRAD_BYTES),
                    help="gradient element type the fused step reads")
+    p.add_argument("--v-nonzero", action="store_true",
+                   help="AdamW: requantize v with no code 0 in groups with a non-zero scale (opt-in rule)")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="time budget of the CPU oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args(argv)
+
+
+def _workload(args):
+    """The named workload; --v-nonzero adds the opt-in v rule to AdamW's hyper-parameters."""
+    import dataclasses
+    from quantized_optimizer_state_gb300 import workloads as wl
+    w = wl.workload(args.workload, args.rho_bits)
+    if getattr(args, "v_nonzero", False):
+        if w.optimizer != "adamw":
+            raise SystemExit("--v-nonzero applies to AdamW workloads only")
+        w = dataclasses.replace(w, hparams=dict(w.hparams, v_nonzero=True))
+    return w
 
 
 def _dist_env():
@@ -147,7 +161,9 @@ class OracleSample:
         import oracle
         hp = self.w.hparams
         if self.w.optimizer == "adamw":
-            f = lambda c: oracle.adamw_step([c[0]], [c[1]], hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], t)
+            vnz = bool(hp.get("v_nonzero", False))
+            f = lambda c: oracle.adamw_step([c[0]], [c[1]], hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], t,
+                                            v_nonzero=vnz)
         elif self.w.optimizer == "sgd":
             f = lambda c: oracle.sgd_step([c[0]], [c[1]], hp["lr"], hp["momentum"])
         else:
@@ -179,7 +195,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     from quantized_optimizer_state_gb300 import workloads as wl
-    w = wl.workload(args.workload, args.rho_bits)
+    w = _workload(args)
     s = OracleSample(w, args.rho_bits, args.grad_dtype)
     for t in range(1, args.warmup + 1):
         s.step(t)
@@ -345,7 +361,9 @@ def _stepper_of(w):
 def _make_step(opt, hp, table):
     from quantized_optimizer_state_gb300 import fo
     if opt == "adamw":
-        return lambda t, s: fo.fo_adamw_step(table, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], t, s)
+        vnz = bool(hp.get("v_nonzero", False))
+        return lambda t, s: fo.fo_adamw_step(table, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], t, s,
+                                             v_nonzero=vnz)
     if opt == "sgd":
         return lambda t, s: fo.fo_sgd_step(table, hp["lr"], hp["momentum"], s)
     return lambda t, s: fo.fo_lion_step(table, hp["lr"], hp["beta1"], hp["beta2"], s)
@@ -388,7 +406,7 @@ def run_ours(args):
         return reduce_scalar(x, op, ws, device)
 
     fo.lib()
-    w = wl.workload(args.workload, args.rho_bits)
+    w = _workload(args)
     states, grads = _build_states(w, args.rho_bits, device, args.grad_dtype)
     table = fo.table_of(states, grads)
     step = _stepper(w, table)

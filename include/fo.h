@@ -89,7 +89,14 @@ typedef enum fo_state_kind {
      * quantizer that section "实验结果分析" (Fig. 4, Fig. 5) compares the
      * companded codecs against. For quality studies; the step never uses it. */
     FO_STATE_MOMENTUM_LINEAR = 2, /* INT8 codes of m itself                  */
-    FO_STATE_VARIANCE_LINEAR = 3  /* UINT8 codes of v itself                 */
+    FO_STATE_VARIANCE_LINEAR = 3, /* UINT8 codes of v itself                 */
+    /* FO_STATE_VARIANCE with an opt-in safety rule that the page does not
+     * have (its Algorithm 3 "numerical stability" step is unprinted): in a
+     * group with a non-zero scale s the codes are max(rint(.), 1), so every
+     * decoded v there is at least (s/255)^2 and none is 0. A group whose
+     * largest sqrt(v) rounds to an FP16 scale of 0 still stores codes 0.
+     * Decoding is FO_STATE_VARIANCE's. */
+    FO_STATE_VARIANCE_NONZERO = 5
 } fo_state_kind_t;
 
 #define FO_GROUP 32               /* elements per quantization group            */
@@ -128,8 +135,18 @@ typedef struct fo_tensor {
     int32_t grad_dtype;    /* fo_grad_dtype_t: FO_GRAD_BF16 (0) or FO_GRAD_F32 (1)     */
 } fo_tensor_t;
 
-/* AdamW: lr > 0 finite, 0 <= beta < 1, eps > 0 (weight decay is per row). */
-typedef struct fo_adamw_hparams { double lr, beta1, beta2, eps; } fo_adamw_hparams_t;
+/* AdamW: lr > 0 finite, 0 <= beta < 1, eps > 0 (weight decay is per row).
+ * flags: 0, or FO_ADAMW_V_NONZERO to requantize v with the rule of
+ * FO_STATE_VARIANCE_NONZERO. Without it, an element whose sqrt(v) falls below
+ * 1/510 of its group's scale decodes to v = 0, and the next step divides its
+ * momentum by little more than its newest gradient's share of v (or by eps).
+ * reserved must be 0. */
+#define FO_ADAMW_V_NONZERO 1u
+typedef struct fo_adamw_hparams {
+    double lr, beta1, beta2, eps;
+    uint32_t flags;
+    uint32_t reserved;
+} fo_adamw_hparams_t;
 /* SGD with momentum, dampening 0, no Nesterov, L2 weight decay added to grad. */
 typedef struct fo_sgd_hparams { double lr, momentum; } fo_sgd_hparams_t;
 /* Lion (Chen et al. 2023) with decoupled weight decay. */

@@ -26,6 +26,7 @@ MOMENTUM = 0
 VARIANCE = 1
 MOMENTUM_LINEAR = 2   # group quantization without companding (Fig. 4's comparison)
 VARIANCE_LINEAR = 3
+VARIANCE_NONZERO = 5  # companded v, no code 0 where the group scale is non-zero (opt-in rule)
 GROUP = 32
 
 # -ffp-contract=off: no implicit fused multiply-add (gcc contracts by default on
@@ -65,7 +66,8 @@ class Tensor(ctypes.Structure):
 
 class AdamWHparams(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double),
-                ("beta2", ctypes.c_double), ("eps", ctypes.c_double)]
+                ("beta2", ctypes.c_double), ("eps", ctypes.c_double),
+                ("v_nonzero", ctypes.c_int32), ("pad", ctypes.c_int32)]
 
 
 class SGDHparams(ctypes.Structure):
@@ -221,7 +223,7 @@ def merge(theta_p: np.ndarray, rho: np.ndarray, rho_bits: int = 8) -> np.ndarray
 
 
 def _code_dtype(kind: int):
-    if kind not in (MOMENTUM, VARIANCE, MOMENTUM_LINEAR, VARIANCE_LINEAR):
+    if kind not in (MOMENTUM, VARIANCE, MOMENTUM_LINEAR, VARIANCE_LINEAR, VARIANCE_NONZERO):
         raise ValueError(f"unknown state kind {kind}")
     return np.int8 if kind in (MOMENTUM, MOMENTUM_LINEAR) else np.uint8
 
@@ -294,9 +296,10 @@ def _table(states, grads):
     return rows
 
 
-def adamw_step(states, grads, lr, beta1, beta2, eps, step: int):
-    """One fused FlashAdamW step over the list of states (updated in place)."""
-    hp = AdamWHparams(lr, beta1, beta2, eps)
+def adamw_step(states, grads, lr, beta1, beta2, eps, step: int, v_nonzero: bool = False):
+    """One fused FlashAdamW step over the list of states (updated in place);
+    v_nonzero selects the opt-in rule that keeps a non-zero v off code 0."""
+    hp = AdamWHparams(lr, beta1, beta2, eps, int(v_nonzero), 0)
     rc = lib().oracle_adamw_step(_table(states, grads), len(states), ctypes.byref(hp), step)
     if rc != 0:
         raise ValueError("oracle_adamw_step: bad argument")
@@ -318,7 +321,7 @@ def lion_step(states, grads, lr, beta1, beta2):
 
 def adamw_update_fp32(theta, m, v, g, lr, beta1, beta2, eps, step, weight_decay):
     """The AdamW element update on uncompressed FP32 arrays (in place)."""
-    hp = AdamWHparams(lr, beta1, beta2, eps)
+    hp = AdamWHparams(lr, beta1, beta2, eps, 0, 0)
     g = np.ascontiguousarray(g, dtype=np.float32)
     lib().oracle_adamw_update_fp32(_ptr(theta), _ptr(m), _ptr(v), _ptr(g), theta.size,
                                    ctypes.byref(hp), step, weight_decay)

@@ -281,7 +281,8 @@ static float compand(float x, int kind)
 {
     switch (kind) {
     case ORACLE_MOMENTUM: return oracle_phi_m(x);
-    case ORACLE_VARIANCE: return oracle_phi_v(x);
+    case ORACLE_VARIANCE:
+    case ORACLE_VARIANCE_NONZERO: return oracle_phi_v(x);
     default: return x;
     }
 }
@@ -290,7 +291,8 @@ static float expand(float z, int kind)
 {
     switch (kind) {
     case ORACLE_MOMENTUM: return oracle_phi_m_inv(z);
-    case ORACLE_VARIANCE: return oracle_phi_v_inv(z);
+    case ORACLE_VARIANCE:
+    case ORACLE_VARIANCE_NONZERO: return oracle_phi_v_inv(z);
     default: return z;
     }
 }
@@ -319,6 +321,10 @@ static void quant_group(const float *x, int len, int kind, void *q, uint16_t *sc
                 code = levels;
             if (code < lo)
                 code = lo;
+            /* opt-in safety rule: in a group with a non-zero scale no code is
+             * 0, so no second moment there decodes to 0 (v^ >= (s/255)^2) */
+            if (kind == ORACLE_VARIANCE_NONZERO && code < 1.0f)
+                code = 1.0f;
         }
         if (kind_signed(kind))
             ((int8_t *)q)[i] = (int8_t)code;
@@ -493,6 +499,7 @@ enum { OPT_ADAMW, OPT_SGD, OPT_LION };
 
 typedef struct {
     int opt;
+    int v_kind;   /* ORACLE_VARIANCE, or ORACLE_VARIANCE_NONZERO (AdamW's opt-in rule) */
     adamw_consts_t adamw;
     lion_consts_t lion;
     double lr;
@@ -549,7 +556,7 @@ static void step_group(const oracle_tensor_t *t, int64_t g0, int len, const step
     }
     quant_group(m, len, ORACLE_MOMENTUM, t->m_q + g0, &t->m_scale[gi]);
     if (k->opt == OPT_ADAMW)
-        quant_group(v, len, ORACLE_VARIANCE, t->v_q + g0, &t->v_scale[gi]);
+        quant_group(v, len, k->v_kind, t->v_q + g0, &t->v_scale[gi]);
 }
 
 static int run_step(const oracle_tensor_t *table, int32_t ntensors, const step_consts_t *k)
@@ -576,7 +583,10 @@ int oracle_adamw_step(const oracle_tensor_t *table, int32_t ntensors,
         return -1;
     step_consts_t k;
     memset(&k, 0, sizeof k);
+    if (hp->v_nonzero != 0 && hp->v_nonzero != 1)
+        return -1;
     k.opt = OPT_ADAMW;
+    k.v_kind = hp->v_nonzero ? ORACLE_VARIANCE_NONZERO : ORACLE_VARIANCE;
     k.adamw = adamw_consts(hp, step);
     k.lr = hp->lr;
     return run_step(table, ntensors, &k);

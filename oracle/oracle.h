@@ -25,7 +25,11 @@ extern "C" {
 /* state kinds: the companded codecs of the method, and the same group
  * quantization without companding (the ablation the page compares against in
  * Fig. 4 and Fig. 5): odd kinds are unsigned (second moment), even signed */
-enum { ORACLE_MOMENTUM = 0, ORACLE_VARIANCE = 1, ORACLE_MOMENTUM_LINEAR = 2, ORACLE_VARIANCE_LINEAR = 3 };
+enum { ORACLE_MOMENTUM = 0, ORACLE_VARIANCE = 1, ORACLE_MOMENTUM_LINEAR = 2, ORACLE_VARIANCE_LINEAR = 3,
+       /* the second-moment codec with the opt-in safety rule: in a group
+        * with a non-zero scale the codes are max(rint(.), 1), so no v there
+        * decodes to 0 */
+       ORACLE_VARIANCE_NONZERO = 5 };
 
 /* One row of the parameter table: the compressed state of one tensor. */
 typedef struct oracle_tensor {
@@ -46,7 +50,8 @@ typedef struct oracle_tensor {
 /* Hyper-parameters are doubles (as Python floats are); the per-element
  * arithmetic uses them rounded to FP32, and derived scalars are formed in
  * double and rounded once. */
-typedef struct { double lr, beta1, beta2, eps; } oracle_adamw_hparams_t;
+/* v_nonzero = 1 requantizes v with ORACLE_VARIANCE_NONZERO (opt-in safety rule) */
+typedef struct { double lr, beta1, beta2, eps; int32_t v_nonzero, pad; } oracle_adamw_hparams_t;
 typedef struct { double lr, momentum; } oracle_sgd_hparams_t;
 typedef struct { double lr, beta1, beta2; } oracle_lion_hparams_t;
 

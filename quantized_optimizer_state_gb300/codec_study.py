@@ -1,6 +1,6 @@
 """Codec-quality study: the two quality figures of "FlashOptim: Optimizers for
 Memory Efficient Training", reproduced on synthetic inputs with this
-library's kernels.
+library's kernels, and a measurement of the opt-in second-moment rule.
 
 * Fig. 3 (section "实验结果分析", weight reconstruction): every FP32 value of
   each binade [2^e, 2^(e+1)) is split into theta' + rho and merged back
@@ -16,6 +16,10 @@ library's kernels.
   ``fo_dequant_state``, ``FO_STATE_*`` and ``FO_STATE_*_LINEAR``). Reported:
   quantiles of the per-group normalised squared error
   sum (x - x^)^2 / sum x^2 and the share of groups decoded to all zeros.
+
+* Second-moment safety: the fused AdamW step with and without
+  ``FO_ADAMW_V_NONZERO`` on identical spiky gradients, counting the elements
+  whose v decodes to 0 while their momentum does not, and the largest update.
 
 The codec kernels' throughput is measured on the way (CUDA events, bytes each
 kernel must move). ``python -m quantized_optimizer_state_gb300.codec_study``
@@ -155,6 +159,61 @@ def nmse_study(n_groups: int = 1 << 20, seed: int = 0, device="cuda", decades=(-
     }
 
 
+def zero_v_events(st: "fo.CompressedTensor") -> int:
+    """Elements whose second moment decodes to 0 while their momentum does not
+    (v code 0 in a group with a non-zero scale, m code non-zero): the next step
+    divides a non-zero momentum by sqrt(0) + eps there."""
+    vq = st.v_q.view(-1, 32) if st.numel % 32 == 0 else None
+    if vq is None:
+        raise ValueError("whole groups only")
+    live = (st.v_scale != 0).view(-1, 1)
+    return int(((vq == 0) & live & (st.m_q.view(-1, 32) != 0)).sum().item())
+
+
+def variance_safety_study(n: int = 1 << 22, steps: int = 200, seed: int = 0, device="cuda",
+                          lr: float = 1e-3, spike_prob: float = 1e-4, spike: float = 1e3) -> Dict:
+    """Run the fused AdamW step with and without FO_ADAMW_V_NONZERO on the same
+    gradients: Student-t(3) noise of scale 1e-3 with rare spikes (probability
+    spike_prob, size x spike) that pin a group's v scale for thousands of steps.
+    Reports per mode the zero-decode events per step and the largest update
+    |theta_t - theta_{t-1}| in units of lr."""
+    fo.lib()
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    theta0 = torch.randn(n, device=device, generator=gen) * 0.02
+    modes = {}
+    for name, flag in (("plain", False), ("v_nonzero", True)):
+        st = fo.CompressedTensor(n, device, 8, True, 0.01)
+        st.init_from(theta0)
+        modes[name] = (st, flag, {"events": [], "max_update_lr": [], "p999_update_lr": []})
+    prev = {k: theta0.clone() for k in modes}
+    cur = torch.empty(n, device=device)
+    for t in range(1, steps + 1):
+        z = torch.randn(n, device=device, generator=gen)
+        c = torch.randn(3, n, device=device, generator=gen).square().sum(0)
+        g = z / torch.sqrt(c / 3.0) * 1e-3
+        spikes = torch.rand(n, device=device, generator=gen) < spike_prob
+        g = torch.where(spikes, g * spike, g).to(torch.bfloat16)
+        for name, (st, flag, rec) in modes.items():
+            fo.fo_adamw_step(fo.table_of([st], [g]), lr, 0.9, 0.999, 1e-8, t, v_nonzero=flag)
+            fo.fo_merge(st.theta, st.rho, cur, 8)
+            upd = (cur - prev[name]).abs() / lr
+            rec["events"].append(zero_v_events(st))
+            rec["max_update_lr"].append(upd.max().item())
+            rec["p999_update_lr"].append(torch.quantile(upd[:1 << 20], 0.999).item())
+            prev[name].copy_(cur)
+    out = {"params": n, "steps": steps, "spike_prob": spike_prob, "spike": spike}
+    for name, (_, _, rec) in modes.items():
+        ev = rec["events"]
+        out[name] = {
+            "events_total": int(sum(ev)), "events_last_step": ev[-1],
+            "steps_with_events": int(sum(1 for e in ev if e)),
+            "max_update_lr": max(rec["max_update_lr"]),
+            "p999_update_lr_last": rec["p999_update_lr"][-1],
+        }
+    return out
+
+
 def _time(fn, reps: int) -> float:
     """Mean milliseconds of fn() over reps launches on the current stream."""
     fn()
@@ -213,6 +272,7 @@ def run(quick: bool = False, device="cuda") -> Dict:
         # and over two (every group's v has an FP16 scale)
         "figure4": nmse_study(1 << (14 if quick else 20), 0, device, decades=(-6.0, -1.0)),
         "figure4_fp16_scales": nmse_study(1 << (14 if quick else 20), 1, device, decades=(-2.0, 0.0)),
+        "variance_safety": variance_safety_study(1 << (18 if quick else 22), 50 if quick else 300, 0, device),
         "throughput": codec_throughput(1 << (24 if quick else 28), device),
     }
     return out

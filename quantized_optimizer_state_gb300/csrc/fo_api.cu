@@ -183,7 +183,7 @@ bool beta_ok(double b) { return is_finite(b) && b >= 0.0 && b < 1.0; }
 bool kind_ok(fo_state_kind_t kind)
 {
     return kind == FO_STATE_MOMENTUM || kind == FO_STATE_VARIANCE || kind == FO_STATE_MOMENTUM_LINEAR ||
-           kind == FO_STATE_VARIANCE_LINEAR;
+           kind == FO_STATE_VARIANCE_LINEAR || kind == FO_STATE_VARIANCE_NONZERO;
 }
 
 fo_status_t check_codec(const void *a, const void *b, const void *c, int64_t n)
@@ -261,7 +261,7 @@ fo_status_t fo_adamw_step(const fo_tensor_t *table, int32_t ntensors, const fo_a
     if (step < 1)
         return FO_ERR_SIZE;
     if (!is_finite(hp->lr) || hp->lr < 0.0 || !beta_ok(hp->beta1) || !beta_ok(hp->beta2) || !is_finite(hp->eps) ||
-        hp->eps <= 0.0)
+        hp->eps <= 0.0 || (hp->flags & ~FO_ADAMW_V_NONZERO) != 0 || hp->reserved != 0)
         return FO_ERR_BAD_ARG;
     const double bc1 = 1.0 - pow_by_squaring(hp->beta1, step);
     const double bc2 = 1.0 - pow_by_squaring(hp->beta2, step);
@@ -285,6 +285,7 @@ fo_status_t fo_adamw_step(const fo_tensor_t *table, int32_t ntensors, const fo_a
     // /sqrt(bc2) + eps stays in [2^-40, 2^40] when these hold (|g| <= 2^24 is
     // checked per element)
     s.fast = (s.a[4] >= 0x1p-40f && s.a[4] <= 0x1p20f && s.a[6] <= 0x1p8f) ? 1 : 0;
+    s.v_nonzero = (hp->flags & FO_ADAMW_V_NONZERO) ? 1 : 0;
     return run_table(Opt::kAdamW, table, ntensors, s, hp->lr, decay_coef, stream);
 }
 

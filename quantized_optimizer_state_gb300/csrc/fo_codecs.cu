@@ -156,11 +156,13 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const uint16_t *__restr
 
 // kind 0: momentum (INT8, phi_m); kind 1: second moment (UINT8, phi_v);
 // kinds 2 and 3: the same group quantization without companding (phi the
-// identity), the linear quantizer the page compares against in Fig. 4.
+// identity), the linear quantizer the page compares against in Fig. 4;
+// kind 5: kind 1 with no code 0 in a group whose scale is non-zero.
 template <int Kind>
 struct KindTraits {
     static constexpr bool kSigned = (Kind & 1) == 0;
-    static constexpr bool kCompanded = Kind < 2;
+    static constexpr bool kCompanded = Kind != 2 && Kind != 3;
+    static constexpr bool kNonzero = Kind == 5;
     static constexpr float kLevels = kSigned ? 127.0f : 255.0f;
 };
 
@@ -214,7 +216,9 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const float *__restrict
         uint32_t cw[kEPT];
 #pragma unroll
         for (int j = 0; j < kEPT; ++j)
-            cw[j] = KindTraits<Kind>::kSigned ? m_code(y[j], mult) : v_code(y[j], mult);
+            cw[j] = KindTraits<Kind>::kSigned ? m_code(y[j], mult)
+                    : KindTraits<Kind>::kNonzero ? v_code_nonzero(y[j], mult)
+                                                 : v_code(y[j], mult);
         if (cnt == kEPT) {
             uint32_t o[4];
 #pragma unroll
@@ -323,7 +327,8 @@ cudaError_t launch_quant(const float *x, void *q, uint16_t *scales, int64_t n, i
     case 0: quant_kernel<0><<<grid, kThreads, 0, stream>>>(x, q, scales, n, ck); break;
     case 1: quant_kernel<1><<<grid, kThreads, 0, stream>>>(x, q, scales, n, ck); break;
     case 2: quant_kernel<2><<<grid, kThreads, 0, stream>>>(x, q, scales, n, ck); break;
-    default: quant_kernel<3><<<grid, kThreads, 0, stream>>>(x, q, scales, n, ck); break;
+    case 3: quant_kernel<3><<<grid, kThreads, 0, stream>>>(x, q, scales, n, ck); break;
+    default: quant_kernel<5><<<grid, kThreads, 0, stream>>>(x, q, scales, n, ck); break;
     }
     count_launch();
     return cudaGetLastError();
@@ -338,7 +343,8 @@ cudaError_t launch_dequant(const void *q, const uint16_t *scales, float *x, int6
     case 0: dequant_kernel<0><<<grid, kThreads, 0, stream>>>(q, scales, x, n, ck); break;
     case 1: dequant_kernel<1><<<grid, kThreads, 0, stream>>>(q, scales, x, n, ck); break;
     case 2: dequant_kernel<2><<<grid, kThreads, 0, stream>>>(q, scales, x, n, ck); break;
-    default: dequant_kernel<3><<<grid, kThreads, 0, stream>>>(q, scales, x, n, ck); break;
+    case 3: dequant_kernel<3><<<grid, kThreads, 0, stream>>>(q, scales, x, n, ck); break;
+    default: dequant_kernel<1><<<grid, kThreads, 0, stream>>>(q, scales, x, n, ck); break;   // kind 5 decodes as 1
     }
     count_launch();
     return cudaGetLastError();

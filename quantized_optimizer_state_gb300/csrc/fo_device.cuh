@@ -192,6 +192,12 @@ __device__ __forceinline__ uint32_t v_code_of(float x)
     return round_code(fminf(x, 255.0f));
 }
 __device__ __forceinline__ uint32_t v_code(float r, float mult) { return v_code_of(__fmul_rn(r, mult)); }
+// The same with the opt-in rule: no code 0 in a group whose scale is non-zero
+// (mult > 0); a zero scale keeps codes 0.
+__device__ __forceinline__ uint32_t v_code_nonzero(float r, float mult)
+{
+    return v_code_of(fmaxf(__fmul_rn(r, mult), mult > 0.0f ? 1.0f : 0.0f));
+}
 
 // The same codes through the saturating round-to-nearest-even conversion
 // (one conversion-unit instruction instead of min/max and an add); the low

@@ -51,11 +51,12 @@ static_assert(sizeof(StepRow) == 72, "StepRow layout");
 //  Lion:  p = {b1, b2, 1-b1, 1-b2, -lr}
 // fast = 1 when the call's hyper-parameters keep the fast path's operands in
 // its validated ranges (AdamW: eps in [2^-40, 2^20], 1/sqrt(bc2) <= 2^8).
+// v_nonzero (AdamW): requantize v with no code 0 in a group with a non-zero scale.
 struct StepScalars {
     float a[8];
     unsigned long long p[8];
     int32_t fast;
-    int32_t pad;
+    int32_t v_nonzero;
 };
 
 // Rows per launch: the whole table of one launch travels in the kernel's

@@ -386,7 +386,8 @@ __device__ __forceinline__ int chunk_count(const StepRow &row, int64_t i0)
 }
 
 // One thread's 16 elements of a tile, from data already loaded into L.
-template <Opt O, int RB, int GB>
+// VNZ (AdamW): requantize v with no code 0 in groups with a non-zero scale.
+template <Opt O, int RB, int GB, bool VNZ>
 __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalars &s, int64_t i0, int cnt,
                                             Loaded &L)
 {
@@ -501,6 +502,7 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
     if (WithV) {
         // r * (255/s) = (-r) * (-(255/s)), exactly
         const float nmult_v = -mult_v;
+        const float vfloor = mult_v > 0.0f ? 1.0f : 0.0f;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             const f2 xa = mul2(pk(nr[4 * w], nr[4 * w + 1]), splat(nmult_v));
@@ -508,6 +510,13 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
             float x0, x1, x2, x3;
             unpk(xa, x0, x1);
             unpk(xb, x2, x3);
+            if (VNZ) {
+                // at least code 1 in a group with a non-zero scale
+                x0 = fmaxf(x0, vfloor);
+                x1 = fmaxf(x1, vfloor);
+                x2 = fmaxf(x2, vfloor);
+                x3 = fmaxf(x3, vfloor);
+            }
             vo[w] = pack_bytes(v_code_sat(x0), v_code_sat(x1), v_code_sat(x2), v_code_sat(x3));
         }
     }
@@ -549,7 +558,7 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
 
 // One launch: rows of one rho width (RB) and gradient width (GB), walked
 // tile by tile.
-template <Opt O, int RB, int GB>
+template <Opt O, int RB, int GB, bool VNZ>
 __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
 fo_fused_step_kernel(const __grid_constant__ StepParams p)
 {
@@ -567,18 +576,18 @@ fo_fused_step_kernel(const __grid_constant__ StepParams p)
             const int cnt = chunk_count(r, i0);
             Loaded L;
             load_chunk<RB, WithV, GB>(r, i0, cnt, L);
-            thread_step<O, RB, GB>(r, p.s, i0, cnt, L);
+            thread_step<O, RB, GB, VNZ>(r, p.s, i0, cnt, L);
         }
     }
 }
 
-template <Opt O, int RB, int GB>
+template <Opt O, int RB, int GB, bool VNZ>
 int resident_ctas()
 {
     static int cached = 0;
     if (cached == 0) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fo_fused_step_kernel<O, RB, GB>, kStepThreads, 0) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fo_fused_step_kernel<O, RB, GB, VNZ>, kStepThreads, 0) !=
                 cudaSuccess ||
             n < 1)
             n = 1;
@@ -587,12 +596,12 @@ int resident_ctas()
     return cached;
 }
 
-template <Opt O, int RB, int GB>
+template <Opt O, int RB, int GB, bool VNZ = false>
 cudaError_t launch(const StepParams &p, cudaStream_t stream)
 {
-    const long long want = (long long)sm_count() * resident_ctas<O, RB, GB>();
+    const long long want = (long long)sm_count() * resident_ctas<O, RB, GB, VNZ>();
     const int grid = (int)(want < p.total_tiles ? want : p.total_tiles);
-    fo_fused_step_kernel<O, RB, GB><<<grid, kStepThreads, 0, stream>>>(p);
+    fo_fused_step_kernel<O, RB, GB, VNZ><<<grid, kStepThreads, 0, stream>>>(p);
     count_launch();
     return cudaGetLastError();
 }
@@ -601,7 +610,8 @@ template <int RB, int GB>
 cudaError_t launch_opt(Opt opt, const StepParams &p, cudaStream_t stream)
 {
     switch (opt) {
-    case Opt::kAdamW: return launch<Opt::kAdamW, RB, GB>(p, stream);
+    case Opt::kAdamW:
+        return p.s.v_nonzero ? launch<Opt::kAdamW, RB, GB, true>(p, stream) : launch<Opt::kAdamW, RB, GB>(p, stream);
     case Opt::kSgd: return launch<Opt::kSgd, RB, GB>(p, stream);
     default: return launch<Opt::kLion, RB, GB>(p, stream);
     }

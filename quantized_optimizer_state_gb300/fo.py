@@ -20,6 +20,8 @@ FO_STATE_MOMENTUM = 0
 FO_STATE_VARIANCE = 1
 FO_STATE_MOMENTUM_LINEAR = 2   # group quantization without companding (quality studies)
 FO_STATE_VARIANCE_LINEAR = 3
+FO_STATE_VARIANCE_NONZERO = 5  # companded v; no code 0 where the group scale is non-zero (opt-in rule)
+FO_ADAMW_V_NONZERO = 1         # fo_adamw_hparams_t.flags: requantize v with that rule
 FO_MAX_TENSORS = 1 << 20
 
 STATUS = {0: "FO_OK", 1: "FO_ERR_NULL", 2: "FO_ERR_MISALIGNED", 3: "FO_ERR_SIZE",
@@ -51,7 +53,8 @@ class FoTensor(ctypes.Structure):
 
 class AdamWHparams(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double),
-                ("beta2", ctypes.c_double), ("eps", ctypes.c_double)]
+                ("beta2", ctypes.c_double), ("eps", ctypes.c_double),
+                ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
 
 
 class SGDHparams(ctypes.Structure):
@@ -188,8 +191,9 @@ def row(theta, rho, m_q, m_scale, grad, v_q=None, v_scale=None, weight_decay: fl
 
 
 def fo_adamw_step(table: Table, lr: float, beta1: float, beta2: float, eps: float, step: int,
-                  stream=None):
-    hp = AdamWHparams(lr, beta1, beta2, eps)
+                  stream=None, v_nonzero: bool = False):
+    """v_nonzero: the opt-in rule that keeps a non-zero v off code 0 (FO_ADAMW_V_NONZERO)."""
+    hp = AdamWHparams(lr, beta1, beta2, eps, FO_ADAMW_V_NONZERO if v_nonzero else 0, 0)
     _check("fo_adamw_step", lib().fo_adamw_step(table.ptr, table.n, ctypes.addressof(hp), int(step),
                                                 _stream(stream)))
 

@@ -85,7 +85,7 @@ class _FlashOptimizer(torch.optim.Optimizer):
             st["v_scale"] = torch.zeros(ng, dtype=torch.int16, device=p.device)
 
     def _make_reference(self, group: Dict) -> torch.optim.Optimizer:
-        hp = {k: v for k, v in group.items() if k not in ("params", "rho_bits", "compress")}
+        hp = {k: v for k, v in group.items() if k not in ("params", "rho_bits", "compress", "v_nonzero")}
         for p in group["params"]:
             if p.dtype != torch.float32:
                 raise TypeError("compress=False groups keep FP32 parameters")
@@ -215,15 +215,19 @@ class _FlashOptimizer(torch.optim.Optimizer):
 
 
 class FlashAdamW(_FlashOptimizer):
-    """AdamW (decoupled weight decay) with compressed master weight and state."""
+    """AdamW (decoupled weight decay) with compressed master weight and state.
+
+    v_nonzero=True opts into a rule the page does not have: a non-zero second
+    moment is never stored as code 0, which would decode it to 0 and let the
+    momentum drive an update of about lr*m/eps."""
     _kind = "adamw"
     _with_v = True
     _reference = torch.optim.AdamW
 
     def __init__(self, params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01,
-                 rho_bits=8, compress=True):
+                 rho_bits=8, compress=True, v_nonzero=False):
         super().__init__(params, dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay,
-                                      rho_bits=rho_bits, compress=compress))
+                                      rho_bits=rho_bits, compress=compress, v_nonzero=v_nonzero))
 
     @staticmethod
     def _reference_args(hp):
@@ -231,7 +235,8 @@ class FlashAdamW(_FlashOptimizer):
 
     def _launch(self, table, group, t):
         b1, b2 = group["betas"]
-        fo.fo_adamw_step(table, group["lr"], b1, b2, group["eps"], t)
+        fo.fo_adamw_step(table, group["lr"], b1, b2, group["eps"], t,
+                         v_nonzero=bool(group.get("v_nonzero", False)))
 
 
 class FlashSGD(_FlashOptimizer):

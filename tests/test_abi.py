@@ -33,7 +33,7 @@ def test_struct_layout_matches_header():
     # 7 pointers, int64 numel, double weight_decay, int32 rho_bits, int32 grad_dtype
     assert ctypes.sizeof(fo.FoTensor) == 80
     assert fo.FoTensor.numel.offset == 56 and fo.FoTensor.weight_decay.offset == 64
-    assert ctypes.sizeof(fo.AdamWHparams) == 32
+    assert ctypes.sizeof(fo.AdamWHparams) == 40     # 4 doubles, uint32 flags, uint32 reserved
 
 
 def test_status_strings():
@@ -55,6 +55,8 @@ def test_codec_argument_errors():
     assert _call("fo_split", A + 2, A, A, 10, 8, None) == 2             # misaligned
     assert _call("fo_merge", A, A + 8, A, 10, 16, None) == 2
     assert _call("fo_quant_state", A, A, A, 10, 7, None) == 4           # bad kind
+    assert _call("fo_quant_state", A, A, A, 10, 4, None) == 4           # 4 is not a kind
+    assert _call("fo_dequant_state", A, A, A, 10, 6, None) == 4
     assert _call("fo_quant_state", A, A, A + 1, 10, 0, None) == 2       # odd scale address
     assert _call("fo_dequant_state", A, None, A, 10, 1, None) == 1
 
@@ -68,9 +70,9 @@ def _table(**over):
     return fo.FoTensor(**base)
 
 
-def _adamw(rows, step=1, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8):
+def _adamw(rows, step=1, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, flags=0, reserved=0):
     arr = (fo.FoTensor * max(1, len(rows)))(*rows)
-    hp = fo.AdamWHparams(lr, beta1, beta2, eps)
+    hp = fo.AdamWHparams(lr, beta1, beta2, eps, flags, reserved)
     return _call("fo_adamw_step", ctypes.addressof(arr), len(rows), ctypes.addressof(hp), step, None)
 
 
@@ -94,6 +96,9 @@ def test_step_argument_errors():
     assert _adamw([_table()], lr=float("inf")) == 4
     assert _adamw([_table()], beta1=1.0) == 4
     assert _adamw([_table()], eps=0.0) == 4
+    assert _adamw([_table()], flags=2) == 4                        # unknown flag bit
+    assert _adamw([_table()], reserved=1) == 4
+    assert _adamw([_table(numel=0)], flags=fo.FO_ADAMW_V_NONZERO) == 0
     assert _adamw([_table(), _table(numel=-1)]) == 3               # checked before any launch
     hp = fo.AdamWHparams(1e-3, 0.9, 0.999, 1e-8)
     assert _call("fo_adamw_step", None, 3, ctypes.addressof(hp), 1, None) == 1

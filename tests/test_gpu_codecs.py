@@ -104,13 +104,14 @@ def _state_inputs(kind, n, seed):
         x[64:96] = (rng.standard_normal(32) * 1e-9).astype(np.float32)  # subnormal-FP16 scale
         x[96:128] = (rng.standard_normal(32) * 1e3).astype(np.float32)  # large values
         x[128:160] = -1e-30                                    # scale rounds to 0
-    if kind in (fo.FO_STATE_VARIANCE, fo.FO_STATE_VARIANCE_LINEAR):
+    if kind in (fo.FO_STATE_VARIANCE, fo.FO_STATE_VARIANCE_LINEAR, fo.FO_STATE_VARIANCE_NONZERO):
         x = np.abs(x) * np.abs(x)
         x = x.astype(np.float32)
     return x
 
 
-KINDS = [fo.FO_STATE_MOMENTUM, fo.FO_STATE_VARIANCE, fo.FO_STATE_MOMENTUM_LINEAR, fo.FO_STATE_VARIANCE_LINEAR]
+KINDS = [fo.FO_STATE_MOMENTUM, fo.FO_STATE_VARIANCE, fo.FO_STATE_MOMENTUM_LINEAR, fo.FO_STATE_VARIANCE_LINEAR,
+         fo.FO_STATE_VARIANCE_NONZERO]
 
 
 def _signed(kind):

@@ -211,3 +211,32 @@ def test_linear_codec_matches_its_float64_definition(orc, kind, levels, signed):
     assert honest.mean() > 0.5
     ok = np.abs(xh - xg) <= 0.5 * step * (1 + 2.0 ** -10) + np.abs(xg) * 2.0 ** -22
     assert np.all(ok[honest])
+
+
+VNZ = 5   # companded v with the opt-in rule: no code 0 in a group with a non-zero scale
+
+
+def test_nonzero_variance_codec_differs_only_at_zero_codes(orc):
+    """The opt-in rule moves exactly the codes 0 of groups with a non-zero
+    scale up to 1 (every decoded v there is then at least (s/255)^2); scales,
+    all other codes and groups with a zero scale are the plain codec's."""
+    rng = np.random.default_rng(51)
+    g = rng.standard_t(2, 32 * 8192)
+    v = (g * g).astype(np.float32)
+    v[::97] = 0.0
+    v[:32] = 0.0                                  # a group with scale 0
+    v[32:64] = 1e-40                              # its scale rounds to 0 in FP16
+    q0, s0 = orc.quant_state(v, V)
+    q1, s1 = orc.quant_state(v, VNZ)
+    assert np.array_equal(s0, s1)
+    live = np.repeat(s0 != 0, 32)
+    moved = q0 != q1
+    assert moved.sum() > 100                     # heavy tails put many elements below s/510
+    assert np.array_equal(moved, live & (q0 == 0))
+    assert np.all(q1[moved] == 1) and np.all(q1[~live] == 0)
+    d = orc.dequant_state(q1, s1, VNZ)
+    sv = orc.fp16_to_f32_n(s1).astype(np.float64)
+    floor = np.repeat((sv / 255) ** 2, 32)
+    assert np.all(d[live] >= floor[live] * (1 - 2.0 ** -20)) and np.all(d[~live] == 0)
+    # decoding is the plain codec's
+    assert np.array_equal(d, orc.dequant_state(q1, s1, V))

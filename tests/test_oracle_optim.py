@@ -216,3 +216,57 @@ def test_bad_arguments_are_rejected(orc):
     st.rho_bits = 12
     with pytest.raises(ValueError):
         orc.adamw_step([st], [gb], 1e-3, 0.9, 0.999, 1e-8, 1)
+
+
+def _spiky_state(orc, n, seed):
+    """A state after a few AdamW steps of heavy-tailed gradients, so that many
+    groups hold a v far below their group's scale."""
+    rng = np.random.default_rng(seed)
+    st = orc.State.from_fp32((rng.standard_normal(n) * 0.02).astype(np.float32), 8, True, 0.01)
+    for t in range(1, 4):
+        g = wl.to_bf16_bits((rng.standard_t(1.5, n) * 1e-3).astype(np.float32))
+        orc.adamw_step([st], [g], 1e-3, 0.9, 0.999, 1e-8, t)
+    return st, rng
+
+
+def test_v_nonzero_step_changes_only_zero_v_codes(orc):
+    """With the opt-in rule, one step from the same state writes the same
+    theta', rho, m codes and scales; v codes differ only where the plain step
+    writes 0 in a group with a non-zero scale, and there they are 1."""
+    n = 32 * 4096
+    st, rng = _spiky_state(orc, n, 61)
+    g = wl.to_bf16_bits((rng.standard_t(1.5, n) * 1e-3).astype(np.float32))
+    a, b = st.copy(), st.copy()
+    orc.adamw_step([a], [g], 1e-3, 0.9, 0.999, 1e-8, 4)
+    orc.adamw_step([b], [g], 1e-3, 0.9, 0.999, 1e-8, 4, v_nonzero=True)
+    for f in ("theta_p", "rho", "m_q", "m_scale", "v_scale"):
+        assert np.array_equal(getattr(a, f), getattr(b, f)), f
+    moved = a.v_q != b.v_q
+    assert moved.sum() > 10
+    assert np.all((a.v_q[moved] == 0) & (b.v_q[moved] == 1))
+    live = np.repeat(a.v_scale != 0, 32)
+    assert np.array_equal(moved, live & (a.v_q == 0))
+    vdec = orc.dequant_state(b.v_q, b.v_scale, 1)
+    assert np.all(vdec[live] > 0)
+
+
+def test_zero_decoded_v_moves_theta_by_m_over_eps(orc):
+    """The hazard the opt-in rule avoids, as a closed form: an element whose v
+    decodes to 0 while its momentum does not, with a zero gradient, moves by
+    lr/bc1 * (beta1 * m) / eps."""
+    lr, b1, b2, eps, t = 1e-3, 0.9, 0.999, 1e-8, 5
+    st = orc.State.from_fp32(np.full(32, 0.5, np.float32), 8, True, 0.0)
+    st.m_q[:] = 64
+    st.m_scale[:] = orc.fp16_rne(0.01)
+    st.v_q[:] = 0
+    st.v_q[0] = 255
+    st.v_scale[:] = orc.fp16_rne(1e-3)
+    mhat = orc.dequant_state(st.m_q, st.m_scale, 0).astype(np.float64)
+    g = np.zeros(32, np.uint16)
+    orc.adamw_step([st], [g], lr, b1, b2, eps, t)
+    got = orc.merge(st.theta_p, st.rho, 8).astype(np.float64)
+    bc1 = 1 - b1 ** t
+    expect = 0.5 - lr / bc1 * (b1 * mhat[1:]) / eps
+    # to the resolution of the stored weight (8-bit rho: 2^-8/254 relative)
+    assert np.allclose(got[1:], expect, rtol=2.0 ** -8 / 254 * 1.05 + 1e-6)
+    assert np.all(np.abs(got[1:] - 0.5) > 1e5 * lr)   # five orders of magnitude above lr
