@@ -329,22 +329,43 @@ def _measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def flat_offsets(sizes, align=64):
+    """Start offsets (in elements) of consecutive tensors in one flat buffer,
+    each rounded up to a multiple of `align` elements (16-byte aligned for any
+    element size), and the buffer's total length."""
+    offs, at = [], 0
+    for n in sizes:
+        offs.append(at)
+        at += (n + align - 1) // align * align
+    return offs, at
+
+
 def _build_states(w, rho_bits, device, grad_dtype="bf16"):
+    """Compressed state and one gradient per tensor. theta' and the gradients of
+    all rows are views into two flat buffers, so the end-to-end leg copies
+    contiguous ranges."""
     import torch
     from quantized_optimizer_state_gb300 import fo
     from quantized_optimizer_state_gb300 import workloads as wl
+    offs, total = flat_offsets([p.numel for p in w.params])
+    gdt = torch.float32 if grad_dtype == "f32" else torch.bfloat16
+    flat_theta = torch.empty(total, dtype=torch.int16, device=device)
+    flat_grad = torch.empty(total, dtype=gdt, device=device)
     states, grads = [], []
+    gen = wl.grad_fp32_device if grad_dtype == "f32" else wl.grad_bf16_device
     for i, p in enumerate(w.params):
+        o = offs[i]
         d = fo.CompressedTensor(p.numel, device, rho_bits, w.optimizer == "adamw",
-                                w.hparams["weight_decay"])
+                                w.hparams["weight_decay"], theta=flat_theta[o:o + p.numel])
         theta = wl.init_weight_device(p, i, device)
         d.init_from(theta)
         del theta
         states.append(d)
-        gen = wl.grad_fp32_device if grad_dtype == "f32" else wl.grad_bf16_device
-        grads.append(gen(w.grad, w.grad_scale, p.numel, i, 1, device))
+        g = flat_grad[o:o + p.numel]
+        g.copy_(gen(w.grad, w.grad_scale, p.numel, i, 1, device))
+        grads.append(g)
     torch.cuda.synchronize(device)
-    return states, grads
+    return states, grads, {"theta": flat_theta, "grad": flat_grad, "offs": offs}
 
 
 def _stepper(w, table):
@@ -407,7 +428,7 @@ def run_ours(args):
 
     fo.lib()
     w = _workload(args)
-    states, grads = _build_states(w, args.rho_bits, device, args.grad_dtype)
+    states, grads, flat = _build_states(w, args.rho_bits, device, args.grad_dtype)
     table = fo.table_of(states, grads)
     step = _stepper(w, table)
     stream = torch.cuda.current_stream(device)
@@ -454,7 +475,7 @@ def run_ours(args):
     # theta' comes back device -> host; the step runs in between.
     e2e = None
     if not args.no_e2e:
-        e2e = _e2e(w, states, grads, _stepper_of(w), stream, device, args.e2e_steps, t, barrier, reduce, ws)
+        e2e = _e2e(w, states, grads, flat, _stepper_of(w), stream, device, args.e2e_steps, t, barrier, reduce, ws)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -503,44 +524,51 @@ def _chunks(sizes, n_chunks):
     return out
 
 
-def _e2e(w, states, grads, step_fn_of, stream, device, steps, t, barrier, reduce, ws, n_chunks=16):
-    """End to end through the C ABI with host buffers: every step copies all BF16
-    gradients host -> device from pinned memory and the updated BF16 theta' device
-    -> host. The table is cut into chunks of consecutive tensors so that the copy-in
-    of one chunk, the fused step of the previous one and the copy-out of the one
-    before overlap on three streams (the step is independent per tensor)."""
+def _e2e(w, states, grads, flat, step_fn_of, stream, device, steps, t, barrier, reduce, ws, n_chunks=16,
+         piece_bytes=128 << 20):
+    """End to end through the C ABI with host buffers: every step copies all
+    gradients host -> device from pinned memory and the updated BF16 theta'
+    device -> host. The table is cut into chunks of consecutive tensors so that
+    the copy-in of one chunk, the fused step of the previous one and the
+    copy-out of the one before overlap on three streams (the step is independent
+    per tensor). theta' and the gradients live in flat buffers, so each chunk's
+    copies are contiguous ranges, issued in pieces of piece_bytes. On the GB300
+    box that keeps both link directions busy at once, where whole-tensor copies
+    of up to 1 GB did not overlap."""
     import torch
-    import torch.distributed as dist
     from quantized_optimizer_state_gb300 import fo
     sizes = [p.numel for p in w.params]
-    offs = [0]
-    for n in sizes:
-        offs.append(offs[-1] + n)
-    h_grad = torch.empty(offs[-1], dtype=grads[0].dtype, pin_memory=True)
-    h_out = torch.empty(offs[-1], dtype=torch.int16, pin_memory=True)
-    for i, g in enumerate(grads):
-        h_grad[offs[i]:offs[i + 1]].copy_(g)
+    offs = flat["offs"]
+    f_grad, f_theta = flat["grad"], flat["theta"]
+    h_grad = torch.empty(f_grad.numel(), dtype=f_grad.dtype, pin_memory=True)
+    h_out = torch.empty(f_theta.numel(), dtype=torch.int16, pin_memory=True)
+    h_grad.copy_(f_grad)
     chunks = _chunks(sizes, n_chunks)
+    ranges = [(offs[c[0]], offs[c[-1]] + sizes[c[-1]]) for c in chunks]
     steppers = [step_fn_of(fo.table_of([states[i] for i in c], [grads[i] for i in c])) for c in chunks]
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     ev_in = [torch.cuda.Event() for _ in chunks]
     ev_done = [torch.cuda.Event() for _ in chunks]
-    h2d = sum(g.element_size() * g.numel() for g in grads)
-    d2h = sum(2 * s.numel for s in states)
+    g_piece = max(1, piece_bytes // f_grad.element_size())
+    t_piece = max(1, piece_bytes // 2)
+    h2d = sum(hi - lo for lo, hi in ranges) * f_grad.element_size()
+    d2h = sum(hi - lo for lo, hi in ranges) * 2
 
     def one(t):
-        for c, idx in enumerate(chunks):
+        for c, (lo, hi) in enumerate(ranges):
             with torch.cuda.stream(s_in):
-                for i in idx:
-                    grads[i].copy_(h_grad[offs[i]:offs[i + 1]], non_blocking=True)
+                for a in range(lo, hi, g_piece):
+                    b = min(hi, a + g_piece)
+                    f_grad[a:b].copy_(h_grad[a:b], non_blocking=True)
                 ev_in[c].record(s_in)
             stream.wait_event(ev_in[c])
             steppers[c](t, stream)
             ev_done[c].record(stream)
             s_out.wait_event(ev_done[c])
             with torch.cuda.stream(s_out):
-                for i in idx:
-                    h_out[offs[i]:offs[i + 1]].copy_(states[i].theta, non_blocking=True)
+                for a in range(lo, hi, t_piece):
+                    b = min(hi, a + t_piece)
+                    h_out[a:b].copy_(f_theta[a:b], non_blocking=True)
         # the next step's copy-in overwrites gradients the step has read: order it
         s_in.wait_stream(stream)
         stream.wait_stream(s_out)
@@ -561,9 +589,9 @@ def _e2e(w, states, grads, step_fn_of, stream, device, steps, t, barrier, reduce
     ms = reduce(e0.elapsed_time(e1), "max")
     return {"value": job_throughput(ws, w.numel, steps, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps,
-            "path": f"pinned host {str(grads[0].dtype).split('.')[-1]} grads -> device, fused step,"
-                    f" theta' -> pinned host; "
-                    f"{len(chunks)} tensor chunks pipelined on copy-in/compute/copy-out streams"}
+            "path": f"pinned host {str(f_grad.dtype).split('.')[-1]} grads -> device, fused step,"
+                    f" theta' -> pinned host; {len(chunks)} tensor chunks pipelined on copy-in/compute/"
+                    f"copy-out streams, copies in {piece_bytes >> 20} MB pieces of flat buffers"}
 
 
 def main(argv=None):

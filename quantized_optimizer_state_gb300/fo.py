@@ -227,14 +227,22 @@ class CompressedTensor:
     """
 
     def __init__(self, numel: int, device, rho_bits: int = 8, with_v: bool = True,
-                 weight_decay: float = 0.0):
+                 weight_decay: float = 0.0, theta=None):
+        """theta: optional int16 device tensor of numel elements to hold theta'
+        (for example a view into one buffer shared by all rows); it must start on
+        a 16-byte boundary."""
         import torch
         self.numel = int(numel)
         self.rho_bits = int(rho_bits)
         self.weight_decay = float(weight_decay)
         ng = (self.numel + GROUP - 1) // GROUP
         e = lambda dt: torch.empty(self.numel, dtype=dt, device=device)
-        self.theta = e(torch.int16)
+        if theta is not None:
+            if theta.dtype != torch.int16 or theta.numel() != self.numel or theta.data_ptr() % 16:
+                raise ValueError("theta must be a 16-byte aligned int16 tensor of numel elements")
+            self.theta = theta
+        else:
+            self.theta = e(torch.int16)
         self.rho = e(torch.int16 if rho_bits == 16 else torch.int8)
         self.m_q = torch.zeros(self.numel, dtype=torch.int8, device=device)
         self.m_scale = torch.zeros(ng, dtype=torch.int16, device=device)

@@ -94,3 +94,12 @@ def test_algorithmic_bytes_per_param():
     assert bench._algo_bytes(adamw, 8, "f32") == 14.25
     assert bench._algo_bytes(lion, 8) == 2 + 2 * (2 + 1 + 1 + 2 / 32)
     assert bench._algo_bytes(lion, 16, "f32") == 4 + 2 * (2 + 2 + 1 + 2 / 32)
+
+
+def test_flat_offsets_are_aligned_and_disjoint():
+    sizes = [1, 4096, 33, 0, 65537, 8]
+    offs, total = bench.flat_offsets(sizes)
+    assert offs[0] == 0 and all(o % 64 == 0 for o in offs)
+    ends = [o + n for o, n in zip(offs, sizes)]
+    assert all(e <= o2 for e, o2 in zip(ends, offs[1:])) and ends[-1] <= total
+    assert total - sum(sizes) < 64 * len(sizes)
