@@ -30,6 +30,12 @@ constexpr int kEPT = kElemsPerThread;
 
 constexpr int kStepMinBlocks = FO_STEP_MIN_BLOCKS;
 
+// codes of groups with normal FP16 scales rounded by a magic-number FADD or by
+// the saturating conversion: bit 0 for m codes, bit 1 for v codes
+#ifndef FO_CODE_FADD
+#define FO_CODE_FADD 1
+#endif
+
 
 struct Loaded {
     uint32_t g[16];  // 16 gradients: BF16 pairs in g[0..7], or FP32 in g[0..15]
@@ -489,35 +495,49 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
     const float s_m = scale_value(sm_new), s_v = scale_value(sv_new);
     const float mult_m = s_m > 0.0f ? div1(127.0f, s_m) : 0.0f;
     const float mult_v = (WithV && s_v > 0.0f) ? div1(255.0f, s_v) : 0.0f;
+    // codes: clamp(rint(x)), x = RN(phi * (L/s)). With s a normal FP16 value
+    // below the 65504 cap the group maximum is at most s*(1 + 2^-11), so x lies
+    // in [-127.07, 127.07] (m) or [0, 255.13] (v): no clamp can apply, and rint is the magic-number addition on the FMA pipe
+    // (the scalar __fadd_rn, never contracted with the product), the code in
+    // the low byte. Subnormal or capped scales take the saturating conversion
+    // on the conversion unit.
+    const bool fadd_m = (FO_CODE_FADD & 1) && (s_m == 0.0f || (s_m >= 0x1p-14f && s_m < 65504.0f));
+    const bool fadd_v = (FO_CODE_FADD & 2) && (s_v == 0.0f || (s_v >= 0x1p-14f && s_v < 65504.0f));
     uint32_t mo[4], vo[4];
+    if (fadd_m) {
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        const f2 xa = mul2(pk(z[4 * w], z[4 * w + 1]), splat(mult_m));
-        const f2 xb = mul2(pk(z[4 * w + 2], z[4 * w + 3]), splat(mult_m));
-        float x0, x1, x2, x3;
-        unpk(xa, x0, x1);
-        unpk(xb, x2, x3);
-        mo[w] = pack_bytes(m_code_sat(x0), m_code_sat(x1), m_code_sat(x2), m_code_sat(x3));
+        for (int w = 0; w < 4; ++w) {
+            float x0, x1, x2, x3;
+            unpk(mul2(pk(z[4 * w], z[4 * w + 1]), splat(mult_m)), x0, x1);
+            unpk(mul2(pk(z[4 * w + 2], z[4 * w + 3]), splat(mult_m)), x2, x3);
+            mo[w] = pack_bytes(round_code(x0), round_code(x1), round_code(x2), round_code(x3));
+        }
+    } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            float x0, x1, x2, x3;
+            unpk(mul2(pk(z[4 * w], z[4 * w + 1]), splat(mult_m)), x0, x1);
+            unpk(mul2(pk(z[4 * w + 2], z[4 * w + 3]), splat(mult_m)), x2, x3);
+            mo[w] = pack_bytes(m_code_sat(x0), m_code_sat(x1), m_code_sat(x2), m_code_sat(x3));
+        }
     }
     if (WithV) {
         // r * (255/s) = (-r) * (-(255/s)), exactly
         const float nmult_v = -mult_v;
-        const float vfloor = mult_v > 0.0f ? 1.0f : 0.0f;
+        const float vfloor = mult_v > 0.0f ? 1.0f : 0.0f;   // VNZ: at least code 1 in a live group
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-            const f2 xa = mul2(pk(nr[4 * w], nr[4 * w + 1]), splat(nmult_v));
-            const f2 xb = mul2(pk(nr[4 * w + 2], nr[4 * w + 3]), splat(nmult_v));
             float x0, x1, x2, x3;
-            unpk(xa, x0, x1);
-            unpk(xb, x2, x3);
+            unpk(mul2(pk(nr[4 * w], nr[4 * w + 1]), splat(nmult_v)), x0, x1);
+            unpk(mul2(pk(nr[4 * w + 2], nr[4 * w + 3]), splat(nmult_v)), x2, x3);
             if (VNZ) {
-                // at least code 1 in a group with a non-zero scale
                 x0 = fmaxf(x0, vfloor);
                 x1 = fmaxf(x1, vfloor);
                 x2 = fmaxf(x2, vfloor);
                 x3 = fmaxf(x3, vfloor);
             }
-            vo[w] = pack_bytes(v_code_sat(x0), v_code_sat(x1), v_code_sat(x2), v_code_sat(x3));
+            vo[w] = fadd_v ? pack_bytes(round_code(x0), round_code(x1), round_code(x2), round_code(x3))
+                           : pack_bytes(v_code_sat(x0), v_code_sat(x1), v_code_sat(x2), v_code_sat(x3));
         }
     }
 
