@@ -9,6 +9,7 @@
 // every thread so that the pair shuffle always has both lanes present.
 #include "fo_device.cuh"
 #include "fo_internal.h"
+#include "fo_pair.cuh"
 
 namespace fo {
 namespace {
@@ -126,12 +127,32 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const uint16_t *__restr
                 if (j < cnt)
                     tw[j >> 1] |= (uint32_t)tp[i0 + j] << (16 * (j & 1));
         }
+        if (cnt == kEPT) {
+            // one 16-byte load of 8-bit rho (two of 16-bit), unpacked with sign extension
+            uint32_t rw[8];
+            if (RB == 8) {
+                const uint4 a = ld_stream(static_cast<const int8_t *>(rho) + i0);
+                rw[0] = a.x; rw[1] = a.y; rw[2] = a.z; rw[3] = a.w;
 #pragma unroll
-        for (int j = 0; j < kEPT; ++j) {
-            if (RB == 8)
-                rv[j] = j < cnt ? static_cast<const int8_t *>(rho)[i0 + j] : 0;
-            else
-                rv[j] = j < cnt ? static_cast<const int16_t *>(rho)[i0 + j] : 0;
+                for (int j = 0; j < kEPT; ++j)
+                    rv[j] = (int32_t)(int8_t)(rw[j >> 2] >> (8 * (j & 3)));
+            } else {
+                const uint4 a = ld_stream(static_cast<const int16_t *>(rho) + i0);
+                const uint4 b = ld_stream(static_cast<const int16_t *>(rho) + i0 + 8);
+                rw[0] = a.x; rw[1] = a.y; rw[2] = a.z; rw[3] = a.w;
+                rw[4] = b.x; rw[5] = b.y; rw[6] = b.z; rw[7] = b.w;
+#pragma unroll
+                for (int j = 0; j < kEPT; ++j)
+                    rv[j] = (int32_t)(int16_t)(rw[j >> 1] >> (16 * (j & 1)));
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < kEPT; ++j) {
+                if (RB == 8)
+                    rv[j] = j < cnt ? static_cast<const int8_t *>(rho)[i0 + j] : 0;
+                else
+                    rv[j] = j < cnt ? static_cast<const int16_t *>(rho)[i0 + j] : 0;
+            }
         }
         float x[kEPT];
 #pragma unroll
@@ -180,6 +201,15 @@ __device__ __forceinline__ float expand(float d)
     if (!KindTraits<Kind>::kCompanded)
         return d;
     return KindTraits<Kind>::kSigned ? phi_m_inv(d) : __fmul_rn(d, d);
+}
+
+// phi_m^-1(z) = z / (2 - |z|) for |z| < 2: the divisor lies in [2^-23, 2]
+// and the quotient is 0 or at least 2^-33 in magnitude (|z| >= 2^-24/127),
+// inside the validated range of div1 (the correctly rounded division of
+// fo_pair.cuh)
+__device__ __forceinline__ float phi_m_inv_fast(float z)
+{
+    return div1(z, __fsub_rn(2.0f, fabsf(z)));
 }
 
 template <int Kind>
@@ -257,7 +287,12 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const void *__restric
                 if (j < cnt)
                     w[j >> 2] |= (uint32_t)static_cast<const uint8_t *>(q)[i0 + j] << (8 * (j & 3));
         }
-        const float step = __fdiv_rn(scale_value(scales[i0 >> 5]), KindTraits<Kind>::kLevels);
+        const uint16_t sbits = scales[i0 >> 5];
+        const float step = __fdiv_rn(scale_value(sbits), KindTraits<Kind>::kLevels);
+        // 0 < s < 1.984375 (FP16 0x0001..0x3FEF): |z| <= 128 * s/127 < 2 for
+        // every byte, -128 included, and z = code * step is never -0 (the fast
+        // division would return +0 for it where IEEE division keeps -0)
+        const bool small_scale = (uint32_t)sbits - 1u < 0x3FEFu;
         float x[kEPT];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -272,7 +307,7 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const void *__restric
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float d = __fmul_rn(cc[e], step);
-                x[4 * k + e] = expand<Kind>(d);
+                x[4 * k + e] = (Kind == 0 && small_scale) ? phi_m_inv_fast(d) : expand<Kind>(d);
             }
         }
         if (cnt == kEPT) {

@@ -146,3 +146,27 @@ def test_dequant_matches_oracle(kind, n):
     out = torch.empty(n, device="cuda")
     fo.fo_dequant_state(to_dev(q), to_dev(s), out, kind)
     assert_exact(to_host(out), oracle.dequant_state(q, s, kind), "decoded state")
+
+
+def test_dequant_momentum_at_the_fast_path_boundary():
+    """Codes including -128 (never written by the codec, but any byte may be
+    passed) with scales on both sides of FP16 1.984375, where decoding switches
+    between the fast division and the IEEE one: identical to the oracle."""
+    rng = np.random.default_rng(77)
+    n = 32 * 4096
+    q = rng.integers(-128, 128, n).astype(np.int8)
+    q[::7] = -128
+    s = rng.integers(0x3F00, 0x4001, n // 32).astype(np.uint16)
+    out = torch.empty(n, device="cuda")
+    fo.fo_dequant_state(to_dev(q), to_dev(s), out, fo.FO_STATE_MOMENTUM)
+    assert_exact(to_host(out), oracle.dequant_state(q, s, fo.FO_STATE_MOMENTUM), "decoded momentum")
+
+
+def test_dequant_momentum_keeps_the_sign_of_zero():
+    """A zero scale (and a negative-zero scale) decode codes to signed zeros
+    exactly as IEEE division does: -0 for negative codes."""
+    q = np.tile(np.arange(-127, 128, 8, dtype=np.int8), 4)[:32 * 4]
+    s = np.array([0x0000, 0x8000, 0x0001, 0x3C00], np.uint16)
+    out = torch.empty(q.size, device="cuda")
+    fo.fo_dequant_state(to_dev(q), to_dev(s), out, fo.FO_STATE_MOMENTUM)
+    assert_exact(to_host(out), oracle.dequant_state(q, s, fo.FO_STATE_MOMENTUM), "signed zeros")
