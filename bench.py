@@ -288,11 +288,16 @@ def _gpu_id_for_smi(device_index: int) -> str:
 PROFILE = os.path.join(ROOT, "profiles", "fo_fused_step_kernel_adamw_llama31_8b.md")
 
 
+STEP_SOURCES = ("fo_api.cu", "fo_device.cuh", "fo_internal.h", "fo_pair.cuh", "fo_step.cu")
+
+
 def _kernel_source_hash() -> str:
-    """sha256 (first 16 hex digits) of the CUDA sources and the C header."""
-    import glob
+    """sha256 (first 16 hex digits) of the sources that build and launch the
+    fused step kernel (the codec kernels' file is not among them) and the C
+    header."""
     import hashlib
-    files = sorted(glob.glob(os.path.join(ROOT, "quantized_optimizer_state_gb300", "csrc", "*")))
+    csrc = os.path.join(ROOT, "quantized_optimizer_state_gb300", "csrc")
+    files = [os.path.join(csrc, f) for f in STEP_SOURCES]
     files.append(os.path.join(ROOT, "include", "fo.h"))
     h = hashlib.sha256()
     for f in files:
