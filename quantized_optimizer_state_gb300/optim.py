@@ -46,6 +46,8 @@ class _FlashOptimizer(torch.optim.Optimizer):
         defaults.setdefault("compress", True)
         super().__init__(params, defaults)
         self._fallback: Dict[int, torch.optim.Optimizer] = {}
+        # built tables, reused while every pointer in them is unchanged
+        self._tables: Dict[tuple, tuple] = {}
         for gi, group in enumerate(self.param_groups):
             if group["rho_bits"] not in (8, 16):
                 raise ValueError("rho_bits must be 8 or 16")
@@ -76,7 +78,7 @@ class _FlashOptimizer(torch.optim.Optimizer):
             raise TypeError("parameters must be float32 (split on first use) or bfloat16")
         ng = (n + _GROUP - 1) // _GROUP
         st = self.state[p]
-        st["step"] = torch.zeros((), dtype=torch.int64)
+        st["step"] = 0          # a Python int: the step counter t of this parameter
         st["rho"] = rho
         st["m_q"] = torch.zeros(n, dtype=torch.int8, device=p.device)
         st["m_scale"] = torch.zeros(ng, dtype=torch.int16, device=p.device)
@@ -91,17 +93,34 @@ class _FlashOptimizer(torch.optim.Optimizer):
                 raise TypeError("compress=False groups keep FP32 parameters")
         return self._reference(group["params"], **self._reference_args(hp))
 
-    def _row(self, p: torch.Tensor, group: Dict) -> fo.FoTensor:
-        st = self.state[p]
+    @staticmethod
+    def _grad_of(p: torch.Tensor) -> torch.Tensor:
         g = p.grad
         if g.dtype != torch.bfloat16:
             g = g.to(torch.bfloat16)
         if not g.is_contiguous():
             g = g.contiguous()
-        st["_grad_keepalive"] = g
+        return g
+
+    def _row(self, p: torch.Tensor, g: torch.Tensor, group: Dict) -> fo.FoTensor:
+        st = self.state[p]
         return fo.row(_bits16(p.data), st["rho"], st["m_q"], st["m_scale"], _bits16(g),
                       st.get("v_q"), st.get("v_scale"), self._weight_decay(group),
                       group["rho_bits"], p.numel())
+
+    def _table(self, ps: List[torch.Tensor], grads: List[torch.Tensor], group: Dict) -> fo.Table:
+        """The table of these parameters, rebuilt only when a pointer, the
+        weight decay or the correction width changed since the last call."""
+        key = (id(group), tuple(id(p) for p in ps))
+        ptrs = (self._weight_decay(group), group["rho_bits"],
+                tuple(p.data_ptr() for p in ps), tuple(g.data_ptr() for g in grads),
+                tuple(self.state[p]["m_q"].data_ptr() for p in ps))
+        hit = self._tables.get(key)
+        if hit is not None and hit[0] == ptrs:
+            return hit[1]
+        table = fo.Table([self._row(p, g, group) for p, g in zip(ps, grads)])
+        self._tables[key] = (ptrs, table)
+        return table
 
     def _weight_decay(self, group: Dict) -> float:
         return float(group.get("weight_decay", 0.0))
@@ -129,13 +148,11 @@ class _FlashOptimizer(torch.optim.Optimizer):
         by_step: Dict[int, List[torch.Tensor]] = {}
         for p in params:
             st = self.state[p]
-            st["step"] += 1
-            by_step.setdefault(int(st["step"]), []).append(p)
+            st["step"] = int(st["step"]) + 1
+            by_step.setdefault(st["step"], []).append(p)
         for t, ps in by_step.items():
-            table = fo.Table([self._row(p, group) for p in ps])
-            self._launch(table, group, t)
-            for p in ps:
-                self.state[p].pop("_grad_keepalive", None)
+            grads = [self._grad_of(p) for p in ps]     # alive until the launch is enqueued
+            self._launch(self._table(ps, grads, group), group, t)
 
     def _launch(self, table: fo.Table, group: Dict, t: int) -> None:
         raise NotImplementedError
@@ -188,6 +205,10 @@ class _FlashOptimizer(torch.optim.Optimizer):
                 if cur is not None and (cur.dtype != v.dtype or cur.shape != v.shape):
                     raise ValueError(f"state '{n}' does not match the parameter's layout")
                 self.state[p][n] = v.to(device=p.device).clone()
+        for st in self.state.values():
+            if "step" in st:
+                st["step"] = int(st["step"])    # checkpoints may hold it as a tensor
+        self._tables.clear()
 
     # -- export ---------------------------------------------------------------
 

@@ -152,3 +152,31 @@ def test_uncompressed_group_is_standard_adamw():
         topt.step()
     assert w2.dtype == torch.float32 and torch.equal(w2.data, ref.data)
     assert w1.dtype == torch.bfloat16
+
+
+def test_cached_table_with_in_place_grads_and_changed_weight_decay():
+    """Gradients written in place keep every pointer, so the step reuses its
+    table; changing a group's weight decay between steps must still take
+    effect. The second-moment floor is on. Checked against the oracle at
+    every step."""
+    params = _params(7)
+    master0 = [p.detach().clone() for p in params]
+    opt = optim.FlashAdamW(params, lr=1e-3, weight_decay=0.01, v_nonzero=True)
+    ref = _oracle_states(master0, 8, True, 0.01)
+    for p in params:
+        p.grad = torch.zeros(p.shape, dtype=torch.bfloat16, device="cuda")
+    rng = np.random.default_rng(8)
+    for t in range(1, 5):
+        if t == 3:
+            opt.param_groups[0]["weight_decay"] = 0.1
+            for r in ref:
+                r.weight_decay = 0.1
+        grads = [wl.to_bf16_bits((rng.standard_t(3, p.numel()) * 1e-3).astype(np.float32)) for p in params]
+        for p, gb in zip(params, grads):
+            p.grad.view(torch.int16).view(-1).copy_(torch.from_numpy(gb.view(np.int16)))
+        opt.step()
+        oracle.adamw_step(ref, grads, 1e-3, 0.9, 0.999, 1e-8, t, v_nonzero=True)
+        torch.cuda.synchronize()
+        for p, r in zip(params, ref):
+            assert_state_matches(_device_view(opt, p), r, f"cached table step {t}")
+    assert len(opt._tables) == 1
