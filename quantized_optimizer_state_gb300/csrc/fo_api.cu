@@ -126,6 +126,20 @@ fo_status_t run_table(Opt opt, const fo_tensor_t *table, int32_t ntensors, const
     for (int combo = 0; combo < 4; ++combo) {
         const int rb = (combo & 1) ? 16 : 8;
         const int gdt = (combo & 2) ? FO_GRAD_F32 : FO_GRAD_BF16;
+        // chunks per tile for this combination's rows: long tiles for large
+        // tables, shorter ones while the table would give a resident CTA
+        // fewer than kMinTilesPerCta tiles
+        int64_t total = 0;
+        for (int32_t j = 0; j < ntensors; ++j)
+            if (table[j].rho_bits == rb && table[j].grad_dtype == gdt)
+                total += table[j].numel;
+        if (total == 0)
+            continue;
+        const int64_t want_tiles = (int64_t)fo::sm_count() * fo::kStepCtasPerSm * fo::kMinTilesPerCta;
+        const int chunks = total / ((int64_t)fo::kStepChunk * fo::kLongChunks) >= want_tiles ? fo::kLongChunks
+                                                                                            : fo::kShortChunks;
+        p.chunks = chunks;
+        const int64_t tile_elems = (int64_t)fo::kStepChunk * chunks;
         int32_t i = 0;
         while (i < ntensors) {
             int nrows = 0;
@@ -136,7 +150,7 @@ fo_status_t run_table(Opt opt, const fo_tensor_t *table, int32_t ntensors, const
                     ++i;
                     continue;
                 }
-                const int64_t rt = (t.numel + fo::kStepTile - 1) / fo::kStepTile;
+                const int64_t rt = (t.numel + tile_elems - 1) / tile_elems;
                 if (nrows > 0 && tiles + rt > INT32_MAX)
                     break;
                 fo::StepRow &r = p.rows[nrows];

@@ -13,14 +13,16 @@ constexpr int kElemsPerThread = 16;  // one thread holds half a group
 #define FO_STEP_THREADS 256
 #endif
 constexpr int kStepThreads = FO_STEP_THREADS;
-// chunks of kStepThreads * kElemsPerThread elements a CTA steps per tile (the
-// row lookup and per-row constants are shared by a tile's chunks)
-#ifndef FO_STEP_CHUNKS
-#define FO_STEP_CHUNKS 2
-#endif
-constexpr int kStepChunks = FO_STEP_CHUNKS;
 constexpr int kStepChunk = kStepThreads * kElemsPerThread;  // 4096 elements
-constexpr int kStepTile = kStepChunk * kStepChunks;
+// A tile is `chunks` consecutive chunks of one row, stepped by one CTA one
+// after the other (they share the row lookup and per-row constants). The
+// kernel is compiled for kLongChunks and kShortChunks chunks per tile; the
+// host takes the long tiles when they still give every resident CTA at least
+// kMinTilesPerCta tiles (large tables), the short ones otherwise.
+constexpr int kLongChunks = 8;
+constexpr int kShortChunks = 2;
+constexpr int kMinTilesPerCta = 8;
+constexpr int kStepCtasPerSm = 3;   // the step kernel's register budget (80 per thread)
 
 enum class Opt : int { kAdamW = 0, kSgd = 1, kLion = 2 };
 
@@ -67,6 +69,8 @@ struct StepParams {
     StepScalars s;
     int32_t nrows;
     int32_t total_tiles;
+    int32_t chunks;                    // chunks per tile: kLongChunks or kShortChunks
+    int32_t pad;
     int32_t tile_end[kRowsPerLaunch];  // inclusive prefix sums of tiles per row
     StepRow rows[kRowsPerLaunch];
 };

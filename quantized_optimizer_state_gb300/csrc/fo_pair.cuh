@@ -79,8 +79,10 @@ __device__ __forceinline__ float rsqrt_approx(float x)
 }
 
 // RN(a / b) in both lanes, given nb = -b. Valid when b is in [2^-100, 2^100],
-// a is +0 or has |a| >= 2^-100 (or b == 1 exactly), and the quotient is in
-// [2^-100, 2^100] or 0. q0 (the first quotient) is returned for range checks.
+// a is +0 or has |a| >= 2^-100, and the quotient is in [2^-100, 2^100] or 0;
+// also for any a when b is 1/2 or 1 exactly (the refined reciprocal is then
+// exactly 1/b, q0 = a/b exactly and the remainder is 0). q0 (the first
+// quotient) is returned for range checks.
 __device__ __forceinline__ f2 div2(f2 a, f2 nb, f2 &q0)
 {
     float n0, n1;

@@ -24,11 +24,7 @@ namespace {
 constexpr int kEPT = kElemsPerThread;
 // resident CTAs per SM the register budget is sized for (3: 80 registers a
 // thread, which the fast path needs without spilling)
-#ifndef FO_STEP_MIN_BLOCKS
-#define FO_STEP_MIN_BLOCKS 3
-#endif
-
-constexpr int kStepMinBlocks = FO_STEP_MIN_BLOCKS;
+constexpr int kStepMinBlocks = kStepCtasPerSm;
 
 // codes of groups with normal FP16 scales rounded by a magic-number FADD or by
 // the saturating conversion: bit 0 for m codes, bit 1 for v codes
@@ -303,12 +299,16 @@ __device__ __forceinline__ f2 mhat_pair(const uint32_t (&mx)[4], const PairConst
     return div2(zq, pk(__fsub_rn(fabsf(a0), 2.0f), __fsub_rn(fabsf(a1), 2.0f)));
 }
 
-// z = phi_m(m) = 2m / (1 + |m|), packed.
+// z = phi_m(m) = RN(2m / RN(1 + |m|)), packed, as RN(m / (RN(1 + |m|)/2)):
+// halving is exact and commutes with rounding (the divisor is at least 1/2),
+// so the quotient is the same real number without forming 2m (the fast path
+// keeps |m| far below 2^127, where 2m would overflow). The halved divisor is
+// one fma, RN(-0.5*|m| - 0.5) = -RN(1 + |m|)/2.
 __device__ __forceinline__ f2 phi_m_pair(f2 m)
 {
     float m0, m1;
     unpk(m, m0, m1);
-    return div2(add2(m, m), pk(__fsub_rn(-fabsf(m0), 1.0f), __fsub_rn(-fabsf(m1), 1.0f)));
+    return div2(m, pk(__fmaf_rn(-0.5f, fabsf(m0), -0.5f), __fmaf_rn(-0.5f, fabsf(m1), -0.5f)));
 }
 
 
@@ -577,8 +577,8 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
 }
 
 // One launch: rows of one rho width (RB) and gradient width (GB), walked
-// tile by tile.
-template <Opt O, int RB, int GB, bool VNZ>
+// tile by tile, CH chunks per tile.
+template <Opt O, int RB, int GB, bool VNZ, int CH>
 __global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
 fo_fused_step_kernel(const __grid_constant__ StepParams p)
 {
@@ -589,11 +589,15 @@ fo_fused_step_kernel(const __grid_constant__ StepParams p)
             ++row;
         const int first = row == 0 ? 0 : p.tile_end[row - 1];
         const StepRow &r = p.rows[row];
-        const int64_t t0 = (int64_t)(tile - first) * kStepTile + (int64_t)threadIdx.x * kEPT;
+        const int64_t t0 = (int64_t)(tile - first) * CH * kStepChunk + (int64_t)threadIdx.x * kEPT;
 #pragma unroll 1
-        for (int c = 0; c < kStepChunks; ++c) {
+        for (int c = 0; c < CH; ++c) {
             const int64_t i0 = t0 + (int64_t)c * kStepChunk;
             const int cnt = chunk_count(r, i0);
+            // a warp entirely past the tensor's end has nothing to do (a
+            // warp-uniform exit: no lane is left waiting on the group shuffle)
+            if (__all_sync(0xFFFFFFFFu, cnt <= 0))
+                break;
             Loaded L;
             load_chunk<RB, WithV, GB>(r, i0, cnt, L);
             thread_step<O, RB, GB, VNZ>(r, p.s, i0, cnt, L);
@@ -601,13 +605,13 @@ fo_fused_step_kernel(const __grid_constant__ StepParams p)
     }
 }
 
-template <Opt O, int RB, int GB, bool VNZ>
+template <Opt O, int RB, int GB, bool VNZ, int CH>
 int resident_ctas()
 {
     static int cached = 0;
     if (cached == 0) {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fo_fused_step_kernel<O, RB, GB, VNZ>, kStepThreads, 0) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fo_fused_step_kernel<O, RB, GB, VNZ, CH>, kStepThreads, 0) !=
                 cudaSuccess ||
             n < 1)
             n = 1;
@@ -616,14 +620,21 @@ int resident_ctas()
     return cached;
 }
 
+template <Opt O, int RB, int GB, bool VNZ, int CH>
+cudaError_t launch_ch(const StepParams &p, cudaStream_t stream)
+{
+    const long long want = (long long)sm_count() * resident_ctas<O, RB, GB, VNZ, CH>();
+    const int grid = (int)(want < p.total_tiles ? want : p.total_tiles);
+    fo_fused_step_kernel<O, RB, GB, VNZ, CH><<<grid, kStepThreads, 0, stream>>>(p);
+    count_launch();
+    return cudaGetLastError();
+}
+
 template <Opt O, int RB, int GB, bool VNZ = false>
 cudaError_t launch(const StepParams &p, cudaStream_t stream)
 {
-    const long long want = (long long)sm_count() * resident_ctas<O, RB, GB, VNZ>();
-    const int grid = (int)(want < p.total_tiles ? want : p.total_tiles);
-    fo_fused_step_kernel<O, RB, GB, VNZ><<<grid, kStepThreads, 0, stream>>>(p);
-    count_launch();
-    return cudaGetLastError();
+    return p.chunks == kLongChunks ? launch_ch<O, RB, GB, VNZ, kLongChunks>(p, stream)
+                                   : launch_ch<O, RB, GB, VNZ, kShortChunks>(p, stream);
 }
 
 template <int RB, int GB>

@@ -112,3 +112,14 @@ def test_sgd_momentum_above_fast_range():
     theta[1000:1040] = 1e30                      # wd * theta = 1e34: |m| > 2^100
     st2 = oracle.State.from_fp32(theta, 8, False, 1e4)
     _step_and_compare("sgd", st2, g, steps=1)
+
+
+@pytest.mark.parametrize("opt", ["sgd", "lion"])
+def test_tiny_momenta(opt):
+    """Gradients around 1e-33 (momenta below 2^-100, BF16 subnormals among
+    them): companding divides by RN(1 + |m|)/2 = 1/2 exactly, where the fast
+    division is exact for any dividend. Half the tensor tiny, half ordinary."""
+    rng, st, g = _base(9, False)
+    g[: N // 2] = (rng.standard_normal(N // 2) * 1e-33).astype(np.float32)
+    g[N // 2: N // 2 + 64] = (rng.standard_normal(64) * 1e-39).astype(np.float32)   # subnormal in BF16
+    _step_and_compare(opt, st, g, steps=3)
