@@ -26,11 +26,6 @@ constexpr int kEPT = kElemsPerThread;
 // thread, which the fast path needs without spilling)
 constexpr int kStepMinBlocks = kStepCtasPerSm;
 
-// codes of groups with normal FP16 scales rounded by a magic-number FADD or by
-// the saturating conversion: bit 0 for m codes, bit 1 for v codes
-#ifndef FO_CODE_FADD
-#define FO_CODE_FADD 1
-#endif
 
 
 struct Loaded {
@@ -495,22 +490,25 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
     const float s_m = scale_value(sm_new), s_v = scale_value(sv_new);
     const float mult_m = s_m > 0.0f ? div1(127.0f, s_m) : 0.0f;
     const float mult_v = (WithV && s_v > 0.0f) ? div1(255.0f, s_v) : 0.0f;
-    // codes: clamp(rint(x)), x = RN(phi * (L/s)). With s a normal FP16 value
-    // below the 65504 cap the group maximum is at most s*(1 + 2^-11), so x lies
-    // in [-127.07, 127.07] (m) or [0, 255.13] (v): no clamp can apply, and rint is the magic-number addition on the FMA pipe
-    // (the scalar __fadd_rn, never contracted with the product), the code in
-    // the low byte. Subnormal or capped scales take the saturating conversion
-    // on the conversion unit.
-    const bool fadd_m = (FO_CODE_FADD & 1) && (s_m == 0.0f || (s_m >= 0x1p-14f && s_m < 65504.0f));
-    const bool fadd_v = (FO_CODE_FADD & 2) && (s_v == 0.0f || (s_v >= 0x1p-14f && s_v < 65504.0f));
+    // codes: clamp(rint(x)), x = RN(phi * (L/s)). For m with a normal FP16
+    // scale below the 65504 cap the group maximum is at most s*(1 + 2^-11),
+    // so |x| <= 127.07: no clamp can apply, and rint is the magic-number
+    // addition on the FMA pipe (the code in the low byte). Subnormal or
+    // capped m scales, and all v codes, take the saturating conversion.
+    const bool fadd_m = s_m == 0.0f || (s_m >= 0x1p-14f && s_m < 65504.0f);
     uint32_t mo[4], vo[4];
     if (fadd_m) {
+        // The product is formed as fma(z, 127/s, +0) with a zero the compiler
+        // cannot prove (127/s * 0 is not 0 for an infinite 127/s), so that the
+        // rounding add stays a separate rounding: fusing the two would need
+        // four operands.
+        const f2 zero_m = splat(__fmul_rn(mult_m, 0.0f));
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-            float x0, x1, x2, x3;
-            unpk(mul2(pk(z[4 * w], z[4 * w + 1]), splat(mult_m)), x0, x1);
-            unpk(mul2(pk(z[4 * w + 2], z[4 * w + 3]), splat(mult_m)), x2, x3);
-            mo[w] = pack_bytes(round_code(x0), round_code(x1), round_code(x2), round_code(x3));
+            float c0, c1, c2, c3;
+            unpk(add2(fma2(pk(z[4 * w], z[4 * w + 1]), splat(mult_m), zero_m), splat(kRoundMagic)), c0, c1);
+            unpk(add2(fma2(pk(z[4 * w + 2], z[4 * w + 3]), splat(mult_m), zero_m), splat(kRoundMagic)), c2, c3);
+            mo[w] = pack_bytes(__float_as_uint(c0), __float_as_uint(c1), __float_as_uint(c2), __float_as_uint(c3));
         }
     } else {
 #pragma unroll
@@ -536,8 +534,7 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
                 x2 = fmaxf(x2, vfloor);
                 x3 = fmaxf(x3, vfloor);
             }
-            vo[w] = fadd_v ? pack_bytes(round_code(x0), round_code(x1), round_code(x2), round_code(x3))
-                           : pack_bytes(v_code_sat(x0), v_code_sat(x1), v_code_sat(x2), v_code_sat(x3));
+            vo[w] = pack_bytes(v_code_sat(x0), v_code_sat(x1), v_code_sat(x2), v_code_sat(x3));
         }
     }
 
