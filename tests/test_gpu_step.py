@@ -39,7 +39,8 @@ def _make_states(thetas, opt, rho_bits, weight_decay):
 def _gpu_step(opt, dev_states, dev_grads, t, hp):
     table = fo.table_of(dev_states, dev_grads)
     if opt == "adamw":
-        fo.fo_adamw_step(table, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], t)
+        fo.fo_adamw_step(table, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], t,
+                         v_nonzero=hp.get("v_nonzero", False))
     elif opt == "sgd":
         fo.fo_sgd_step(table, hp["lr"], hp["momentum"])
     else:
@@ -49,7 +50,8 @@ def _gpu_step(opt, dev_states, dev_grads, t, hp):
 
 def _oracle_step(opt, states, grads, t, hp):
     if opt == "adamw":
-        oracle.adamw_step(states, grads, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], t)
+        oracle.adamw_step(states, grads, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], t,
+                          v_nonzero=hp.get("v_nonzero", False))
     elif opt == "sgd":
         oracle.sgd_step(states, grads, hp["lr"], hp["momentum"])
     else:
