@@ -1,15 +1,20 @@
-"""Parity of every step kernel built for long tiles (8 chunks of 4096
-elements), which the library launches for tables large enough to give each
-resident CTA at least 8 such tiles (about 120M elements). Each case is one
-row of 2^27 elements, checked against the oracle on chunks at its head,
-middle and tail over two steps (groups are independent, so a chunk's oracle
-step needs only that chunk's state)."""
+"""Parity of every step kernel, for both tile lengths the library launches.
+
+Long tiles (8 chunks of 4096 elements) are used for tables large enough to
+give each resident CTA at least 8 of them (about 120M elements). Each long
+case is one row of 2^27 elements, checked against the oracle on chunks at its
+head, middle and tail over two steps (groups are independent, so a chunk's
+oracle step needs only that chunk's state). Short tiles (2 chunks) serve
+smaller tables. Each short case is a small ragged table, checked in full."""
 import pytest
 import torch
 
 import oracle
 from quantized_optimizer_state_gb300 import fo
-from tests.test_gpu_step import ADAMW, _sampled_parity, _samples_of
+from quantized_optimizer_state_gb300 import workloads as wl
+import numpy as np
+
+from tests.test_gpu_step import ADAMW, RAGGED, _sampled_parity, _samples_of, run_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -42,3 +47,17 @@ def test_long_tile_kernel(opt, rho_bits, fp32_grad, v_nonzero):
         _sampled_parity(opt, [d], [g], samples, t, hp)
     del d
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("opt,rho_bits,fp32_grad,v_nonzero", CASES)
+def test_short_tile_kernel(opt, rho_bits, fp32_grad, v_nonzero):
+    rng = np.random.default_rng(rho_bits * 7 + fp32_grad * 3 + v_nonzero + 100)
+    thetas = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in RAGGED]
+
+    def grads(t):
+        r = np.random.default_rng(1000 * t + rho_bits)
+        g = [(r.standard_t(3, n) * 1e-3).astype(np.float32) for n in RAGGED]
+        return g if fp32_grad else [wl.to_bf16_bits(x) for x in g]
+    hp = dict(HP[opt], v_nonzero=v_nonzero) if opt == "adamw" else HP[opt]
+    run_parity(opt, thetas, grads, 3, hp, rho_bits, 0.01,
+               f"{opt} rho{rho_bits}{' fp32' if fp32_grad else ''}{' vnz' if v_nonzero else ''}")
