@@ -6,12 +6,17 @@
 //
 // Design (GB300, sm_103a): the work is element-wise plus a 32-wide absmax per
 // group, so it is bound by HBM traffic and instruction issue, never by tensor
-// cores. A persistent grid (SMs x resident CTAs) walks 4096-element tiles of
-// the concatenated tensor list in a static round-robin; a thread owns 16
-// contiguous elements (half a group) and loads them with 128-bit streaming
-// loads, the two threads of a group combine their absmax with one shuffle,
-// and the results leave with 128-bit streaming stores. Tensor rows travel in
-// the kernel parameters, so a step allocates nothing.
+// cores. A persistent grid (SMs x resident CTAs) walks the tiles of the
+// concatenated tensor list in a static round-robin. A tile is 8 (large
+// tables) or 2 (small ones) consecutive 4096-element chunks of one tensor,
+// stepped one after the other. In a chunk, a thread owns 16 contiguous
+// elements (half a group) and loads them with 128-bit streaming loads; the
+// two threads of a group combine their absmax with one shuffle, and the
+// results leave with 128-bit streaming stores. Pairs of elements are computed
+// with packed FP32 instructions and validated fast division and square root;
+// a thread whose operands leave the validated ranges recomputes its 16
+// elements with IEEE operations. Tensor rows travel in the kernel parameters,
+// so a step allocates nothing.
 #include <utility>
 
 #include "fo_device.cuh"
