@@ -72,7 +72,8 @@ class _FlashOptimizer(torch.optim.Optimizer):
         if p.dtype == torch.float32:
             master = p.detach().reshape(-1).contiguous()
             tp = torch.empty(n, dtype=torch.bfloat16, device=p.device)
-            fo.fo_split(master, _bits16(tp), rho, rb)
+            with torch.cuda.device(p.device):
+                fo.fo_split(master, _bits16(tp), rho, rb)
             p.data = tp.view(p.shape)
         elif p.dtype != torch.bfloat16:
             raise TypeError("parameters must be float32 (split on first use) or bfloat16")
@@ -144,15 +145,17 @@ class _FlashOptimizer(torch.optim.Optimizer):
     def _step_params(self, params: List[torch.Tensor], group: Dict) -> None:
         if not params:
             return
-        # parameters of a group that have taken the same number of steps share a call
-        by_step: Dict[int, List[torch.Tensor]] = {}
+        # parameters of a group on the same device that have taken the same
+        # number of steps share a call (a launch only touches its own device)
+        by_key: Dict[tuple, List[torch.Tensor]] = {}
         for p in params:
             st = self.state[p]
             st["step"] = int(st["step"]) + 1
-            by_step.setdefault(st["step"], []).append(p)
-        for t, ps in by_step.items():
+            by_key.setdefault((st["step"], p.device.index), []).append(p)
+        for (t, dev), ps in by_key.items():
             grads = [self._grad_of(p) for p in ps]     # alive until the launch is enqueued
-            self._launch(self._table(ps, grads, group), group, t)
+            with torch.cuda.device(dev):
+                self._launch(self._table(ps, grads, group), group, t)
 
     def _launch(self, table: fo.Table, group: Dict, t: int) -> None:
         raise NotImplementedError
@@ -221,7 +224,8 @@ class _FlashOptimizer(torch.optim.Optimizer):
                 continue
             for p in group["params"]:
                 w = torch.empty(p.numel(), dtype=torch.float32, device=p.device)
-                fo.fo_merge(_bits16(p.data.reshape(-1)), self.state[p]["rho"], w, group["rho_bits"])
+                with torch.cuda.device(p.device):
+                    fo.fo_merge(_bits16(p.data.reshape(-1)), self.state[p]["rho"], w, group["rho_bits"])
                 out[p] = w.view(p.shape)
         return out
 
