@@ -27,9 +27,6 @@ namespace fo {
 namespace {
 
 constexpr int kEPT = kElemsPerThread;
-// resident CTAs per SM the register budget is sized for (3: 80 registers a
-// thread, which the fast path needs without spilling)
-constexpr int kStepMinBlocks = kStepCtasPerSm;
 
 
 
@@ -581,7 +578,7 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
 // One launch: rows of one rho width (RB) and gradient width (GB), walked
 // tile by tile, CH chunks per tile.
 template <Opt O, int RB, int GB, bool VNZ, int CH>
-__global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
+__global__ void __launch_bounds__(kStepThreads, step_ctas_per_sm(O))
 fo_fused_step_kernel(const __grid_constant__ StepParams p)
 {
     constexpr bool WithV = (O == Opt::kAdamW);
