@@ -57,8 +57,8 @@
  * return a non-zero fo_status_t; launch errors return FO_ERR_CUDA. Faults
  * that happen later surface at the caller's next synchronization. Nothing is
  * thrown across the ABI. Calls on distinct streams over disjoint buffers are
- * independent and thread-safe. State buffers are updated in place; `grad`
- * must not overlap any state buffer.
+ * independent and thread-safe. State buffers are updated in place; no two
+ * arrays of one table row (the gradient and the state buffers) may overlap.
  */
 #ifndef FO_H
 #define FO_H
@@ -78,7 +78,7 @@ typedef enum fo_status {
     FO_ERR_BAD_ARG = 4,          /* a flag or hyper-parameter is out of range   */
     FO_ERR_TOO_MANY_TENSORS = 5, /* ntensors exceeds FO_MAX_TENSORS             */
     FO_ERR_CUDA = 6,             /* a CUDA call failed (see fo_last_cuda_error) */
-    FO_ERR_ALIAS = 7             /* grad overlaps a state buffer of its row     */
+    FO_ERR_ALIAS = 7             /* two arrays of one table row overlap         */
 } fo_status_t;
 
 /* Kind of optimizer state coded by fo_quant_state / fo_dequant_state. */

@@ -89,11 +89,17 @@ fo_status_t check_row(const fo_tensor_t &t, bool with_v)
         return FO_ERR_MISALIGNED;
     if ((reinterpret_cast<uintptr_t>(t.m_scale) & 1u) || (with_v && (reinterpret_cast<uintptr_t>(t.v_scale) & 1u)))
         return FO_ERR_MISALIGNED;
-    const int64_t n = t.numel, ng = (n + 31) / 32, gb = (t.grad_dtype == FO_GRAD_F32 ? 4 : 2) * n;
-    if (overlaps(t.grad, gb, t.theta, 2 * n) || overlaps(t.grad, gb, t.rho, n * (t.rho_bits / 8)) ||
-        overlaps(t.grad, gb, t.m_q, n) || overlaps(t.grad, gb, t.m_scale, 2 * ng) ||
-        (with_v && (overlaps(t.grad, gb, t.v_q, n) || overlaps(t.grad, gb, t.v_scale, 2 * ng))))
-        return FO_ERR_ALIAS;
+    // no two arrays of the row may share a byte: the step reads each one and
+    // writes the state arrays in place
+    const int64_t n = t.numel, ng = (n + 31) / 32;
+    const void *ptr[7] = {t.grad, t.theta, t.rho, t.m_q, t.m_scale, t.v_q, t.v_scale};
+    const int64_t bytes[7] = {(t.grad_dtype == FO_GRAD_F32 ? 4 : 2) * n, 2 * n, n * (t.rho_bits / 8), n, 2 * ng,
+                              n, 2 * ng};
+    const int count = with_v ? 7 : 5;
+    for (int a = 0; a < count; ++a)
+        for (int b = a + 1; b < count; ++b)
+            if (overlaps(ptr[a], bytes[a], ptr[b], bytes[b]))
+                return FO_ERR_ALIAS;
     return FO_OK;
 }
 

@@ -92,8 +92,9 @@ __device__ __forceinline__ void load_chunk(const StepRow &row, int64_t i0, int c
         L.g[w] = 0;
 #pragma unroll
     for (int w = 0; w < 4; ++w) { L.m[w] = 0; L.v[w] = 0; }
-    // the group's scales: needed by both lanes of the pair even when this lane
-    // holds no element (the pair splits the per-group divisions)
+    // the group's scales, read only while the group exists (a lane whose
+    // elements all lie past the end holds zero codes, which decode to zero
+    // whatever the scale)
     const bool group_exists = ((i0 >> 5) << 5) < row.numel;
     L.ms = group_exists ? row.ms[i0 >> 5] : (uint16_t)0;
     L.vs = (WithV && group_exists) ? row.vs[i0 >> 5] : (uint16_t)0;

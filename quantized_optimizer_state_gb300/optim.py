@@ -96,16 +96,21 @@ class _FlashOptimizer(torch.optim.Optimizer):
 
     @staticmethod
     def _grad_of(p: torch.Tensor) -> torch.Tensor:
+        """The gradient as the step reads it: BF16 as it is, FP32 as it is
+        (for example with ``Tensor.grad_dtype`` set to float32, which
+        accumulates FP32 gradients for BF16 parameters; the step then uses
+        them unrounded), any other type widened or rounded to FP32."""
         g = p.grad
-        if g.dtype != torch.bfloat16:
-            g = g.to(torch.bfloat16)
+        if g.dtype != torch.bfloat16 and g.dtype != torch.float32:
+            g = g.float()
         if not g.is_contiguous():
             g = g.contiguous()
         return g
 
     def _row(self, p: torch.Tensor, g: torch.Tensor, group: Dict) -> fo.FoTensor:
         st = self.state[p]
-        return fo.row(_bits16(p.data), st["rho"], st["m_q"], st["m_scale"], _bits16(g),
+        grad = _bits16(g) if g.dtype == torch.bfloat16 else g   # float32: fo.GRAD_F32
+        return fo.row(_bits16(p.data), st["rho"], st["m_q"], st["m_scale"], grad,
                       st.get("v_q"), st.get("v_scale"), self._weight_decay(group),
                       group["rho_bits"], p.numel())
 
@@ -114,7 +119,7 @@ class _FlashOptimizer(torch.optim.Optimizer):
         weight decay or the correction width changed since the last call."""
         key = (id(group), tuple(id(p) for p in ps))
         ptrs = (self._weight_decay(group), group["rho_bits"],
-                tuple(p.data_ptr() for p in ps), tuple(g.data_ptr() for g in grads),
+                tuple(p.data_ptr() for p in ps), tuple((g.data_ptr(), g.dtype) for g in grads),
                 tuple(self.state[p]["m_q"].data_ptr() for p in ps))
         hit = self._tables.get(key)
         if hit is not None and hit[0] == ptrs:

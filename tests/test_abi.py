@@ -93,6 +93,14 @@ def test_step_argument_errors():
     # an FP32 gradient spans 4 bytes an element: 100 of them from 304 bytes
     # below rho reach into it (100 BF16 ones would not)
     assert _adamw([_table(grad=(1 << 24) + (1 << 20) - 304, grad_dtype=1)]) == 7
+    # state buffers of one row overlapping each other
+    assert _adamw([_table(m_q=(1 << 24) + 96)]) == 7               # m codes inside theta'
+    assert _adamw([_table(v_scale=(1 << 24) + (3 << 20) + 6)]) == 7  # v scales inside m scales
+    assert _adamw([_table(rho=(1 << 24) + (2 << 20) - 96)]) == 7   # rho's 100 bytes reach m codes
+    assert _adamw([_table(rho=(1 << 24) + (2 << 20) - 96, rho_bits=16)]) == 7
+    # 100 bytes of rho ending 12 bytes short of the m codes: no overlap, so the
+    # next row's error is the one reported (nothing launches)
+    assert _adamw([_table(rho=(1 << 24) + (2 << 20) - 112), _table(numel=-1)]) == 3
     assert _adamw([_table()], lr=float("inf")) == 4
     assert _adamw([_table()], beta1=1.0) == 4
     assert _adamw([_table()], eps=0.0) == 4
@@ -115,6 +123,10 @@ def test_sgd_and_lion_need_no_v():
     # the v pointers are not required; the bad numel is what is reported
     assert _call("fo_sgd_step", ctypes.addressof(arr), 1, ctypes.addressof(sgd), None) == 3
     assert _call("fo_lion_step", ctypes.addressof(arr), 1, ctypes.addressof(lion), None) == 3
+    # SGD and Lion ignore the v buffers, so theirs may coincide with theta'
+    two = (fo.FoTensor * 2)(_table(v_q=1 << 24, v_scale=1 << 24), _table(numel=-1))
+    assert _call("fo_sgd_step", ctypes.addressof(two), 2, ctypes.addressof(sgd), None) == 3
+    assert _adamw([_table(v_q=1 << 24, v_scale=1 << 24)]) == 7
     bad = fo.SGDHparams(-0.1, 0.9)
     assert _call("fo_sgd_step", ctypes.addressof(arr), 1, ctypes.addressof(bad), None) == 4
     badl = fo.LionHparams(1e-4, 0.9, 1.5)

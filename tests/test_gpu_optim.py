@@ -180,3 +180,42 @@ def test_cached_table_with_in_place_grads_and_changed_weight_decay():
         for p, r in zip(params, ref):
             assert_state_matches(_device_view(opt, p), r, f"cached table step {t}")
     assert len(opt._tables) == 1
+
+
+@pytest.mark.skipif(not hasattr(torch.Tensor, "grad_dtype"), reason="this torch has no Tensor.grad_dtype")
+@pytest.mark.parametrize("kind", ["adamw", "lion"])
+def test_fp32_gradients_reach_the_step_unrounded(kind):
+    """With grad_dtype float32, autograd accumulates FP32 gradients for the
+    BF16 parameters; the step must read them as FP32 (the oracle's FP32
+    gradient path), not rounded to BF16. Negative control: the oracle fed
+    the same gradients rounded to BF16 ends in another state."""
+    params = _params(11)
+    master0 = [p.detach().clone() for p in params]
+    if kind == "adamw":
+        opt = optim.FlashAdamW(params, lr=1e-3, weight_decay=0.01)
+    else:
+        opt = optim.FlashLion(params, lr=1e-4, weight_decay=0.01)
+    ref = _oracle_states(master0, 8, kind == "adamw", 0.01)
+    rounded = [r.copy() for r in ref]
+    for p in params:
+        p.grad_dtype = torch.float32
+    rng = np.random.default_rng(12)
+
+    def oracle_step(states, grads, t):
+        if kind == "adamw":
+            oracle.adamw_step(states, grads, 1e-3, 0.9, 0.999, 1e-8, t)
+        else:
+            oracle.lion_step(states, grads, 1e-4, 0.9, 0.99)
+
+    for t in range(1, 4):
+        grads = [(rng.standard_t(3, p.numel()) * 1e-3).astype(np.float32) for p in params]
+        for p, g in zip(params, grads):
+            p.grad = torch.from_numpy(g).cuda().view(p.shape)
+            assert p.grad.dtype == torch.float32
+        opt.step()
+        oracle_step(ref, grads, t)
+        oracle_step(rounded, [wl.to_bf16_bits(g) for g in grads], t)
+        torch.cuda.synchronize()
+        for p, r in zip(params, ref):
+            assert_state_matches(_device_view(opt, p), r, f"{kind} fp32 grad step {t}")
+    assert any(not np.array_equal(_device_view(opt, p).m_q, r.m_q) for p, r in zip(params, rounded))
