@@ -17,18 +17,25 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int sm_count()
 {
-    static int cached[64] = {0};
+    // per device (up to 64), cached after the first successful query; a
+    // failed query is not cached, and its error is consumed so that the
+    // launch reports its own status
+    static std::atomic<int> cached[64];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        (void)cudaGetLastError();
         dev = 0;
-    const int slot = dev & 63;
-    if (cached[slot] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-            n = 1;
-        cached[slot] = n;
     }
-    return cached[slot];
+    std::atomic<int> &slot = cached[dev & 63];
+    int n = slot.load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+            (void)cudaGetLastError();
+            return 1;
+        }
+        slot.store(n, std::memory_order_relaxed);
+    }
+    return n;
 }
 
 }  // namespace fo
@@ -355,7 +362,7 @@ const char *fo_status_string(fo_status_t status)
     case FO_ERR_BAD_ARG: return "FO_ERR_BAD_ARG: a flag or hyper-parameter is out of range";
     case FO_ERR_TOO_MANY_TENSORS: return "FO_ERR_TOO_MANY_TENSORS: ntensors exceeds FO_MAX_TENSORS";
     case FO_ERR_CUDA: return "FO_ERR_CUDA: a CUDA call failed";
-    case FO_ERR_ALIAS: return "FO_ERR_ALIAS: grad overlaps a state buffer";
+    case FO_ERR_ALIAS: return "FO_ERR_ALIAS: two arrays of one table row overlap";
     }
     return "unknown fo_status_t";
 }

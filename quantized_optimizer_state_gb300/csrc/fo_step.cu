@@ -17,6 +17,7 @@
 // a thread whose operands leave the validated ranges recomputes its 16
 // elements with IEEE operations. Tensor rows travel in the kernel parameters,
 // so a step allocates nothing.
+#include <atomic>
 #include <utility>
 
 #include "fo_device.cuh"
@@ -608,16 +609,20 @@ fo_fused_step_kernel(const __grid_constant__ StepParams p)
 template <Opt O, int RB, int GB, bool VNZ, int CH>
 int resident_ctas()
 {
-    static int cached = 0;
-    if (cached == 0) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fo_fused_step_kernel<O, RB, GB, VNZ, CH>, kStepThreads, 0) !=
-                cudaSuccess ||
-            n < 1)
-            n = 1;
-        cached = n;
+    // cached after the first successful query; a failed query is not cached,
+    // and its error is consumed so that the launch reports its own status
+    static std::atomic<int> cached{0};
+    int n = cached.load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fo_fused_step_kernel<O, RB, GB, VNZ, CH>, kStepThreads,
+                                                          0) != cudaSuccess ||
+            n < 1) {
+            (void)cudaGetLastError();
+            return 1;
+        }
+        cached.store(n, std::memory_order_relaxed);
     }
-    return cached;
+    return n;
 }
 
 template <Opt O, int RB, int GB, bool VNZ, int CH>
