@@ -203,14 +203,6 @@ __device__ __forceinline__ float expand(float d)
     return KindTraits<Kind>::kSigned ? phi_m_inv(d) : __fmul_rn(d, d);
 }
 
-// phi_m^-1(z) = z / (2 - |z|) for |z| < 2: the divisor lies in [2^-23, 2]
-// and the quotient is 0 or at least 2^-33 in magnitude (|z| >= 2^-24/127),
-// inside the validated range of div1 (the correctly rounded division of
-// fo_pair.cuh)
-__device__ __forceinline__ float phi_m_inv_fast(float z)
-{
-    return div1(z, __fsub_rn(2.0f, fabsf(z)));
-}
 
 template <int Kind>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const float *__restrict__ xin, void *__restrict__ q,
@@ -313,10 +305,22 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const void *__restric
                 cc[0] = u8_at<0>(wx); cc[1] = u8_at<1>(wx); cc[2] = u8_at<2>(wx); cc[3] = u8_at<3>(wx);
             }
             float x[4];
+            if (Kind == 0 && small_scale) {
+                // phi_m^-1(z) = z / (2 - |z|) on element pairs, |z| < 2: the
+                // divisor lies in [2^-23, 2] and the quotient is 0 or at least
+                // 2^-33 in magnitude (|z| >= 2^-24/127), inside the validated
+                // range of div2 (the correctly rounded division of fo_pair.cuh)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float d = __fmul_rn(cc[e], step);
-                x[e] = (Kind == 0 && small_scale) ? phi_m_inv_fast(d) : expand<Kind>(d);
+                for (int h = 0; h < 2; ++h) {
+                    const f2 d = mul2(pk(cc[2 * h], cc[2 * h + 1]), splat(step));
+                    float d0, d1;
+                    unpk(d, d0, d1);
+                    unpk(div2(d, pk(__fsub_rn(fabsf(d0), 2.0f), __fsub_rn(fabsf(d1), 2.0f))), x[2 * h], x[2 * h + 1]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    x[e] = expand<Kind>(__fmul_rn(cc[e], step));
             }
             if (cnt == 4) {
                 st_stream(xout + i, make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
