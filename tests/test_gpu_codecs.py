@@ -131,6 +131,25 @@ def test_quant_matches_oracle(kind, n):
 
 
 @pytest.mark.parametrize("kind", KINDS)
+def test_quant_input_alignments(kind):
+    """The quant kernel reads 32-byte-aligned input with 256-bit loads and
+    16-byte-aligned input with 128-bit ones: both give the oracle's codes."""
+    n = (1 << 16) + 45
+    x = _state_inputs(kind, n, 7 * kind + 3)
+    buf = torch.zeros(n + 8, device="cuda")
+    for off in (4, 8):                  # 16 and 32 bytes past a 512-byte boundary
+        view = buf[off:off + n]
+        view.copy_(to_dev(x))
+        assert view.data_ptr() % 32 == (16 if off == 4 else 0)
+        q = torch.empty(n, dtype=torch.int8 if _signed(kind) else torch.uint8, device="cuda")
+        s = torch.empty((n + 31) // 32, dtype=torch.int16, device="cuda")
+        fo.fo_quant_state(view, q, s, kind)
+        q_ref, s_ref = oracle.quant_state(x, kind)
+        assert_codes(to_host(q, q_ref.dtype), q_ref, f"codes, offset {4 * off} bytes")
+        assert_scales(to_host(s), s_ref, f"scales, offset {4 * off} bytes")
+
+
+@pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("n", [1, 33, 1000, (1 << 20) + 7])
 def test_dequant_matches_oracle(kind, n):
     rng = np.random.default_rng(n)
