@@ -379,7 +379,6 @@ def _stepper(w, table):
 
 def _stepper_of(w):
     """table -> step(t, stream) for the workload's optimizer."""
-    from quantized_optimizer_state_gb300 import fo
     hp = w.hparams
     return lambda table: _make_step(w.optimizer, hp, table)
 

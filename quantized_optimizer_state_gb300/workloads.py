@@ -20,7 +20,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
-from typing import Callable, List, Sequence
+from typing import List, Sequence
 
 import numpy as np
 
