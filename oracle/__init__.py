@@ -79,9 +79,12 @@ class LionHparams(ctypes.Structure):
 
 
 def lib() -> ctypes.CDLL:
+    """The oracle library: ``liboracle.so``, or the build of a modified
+    oracle.c that the environment variable ORACLE_LIB names (the mutation
+    test points the pins at such builds)."""
     global _lib
     if _lib is None:
-        l = ctypes.CDLL(build())
+        l = ctypes.CDLL(os.environ.get("ORACLE_LIB") or build())
         vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
         f64 = ctypes.c_double
         u16 = ctypes.c_uint16
