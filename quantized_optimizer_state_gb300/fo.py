@@ -114,10 +114,17 @@ def _check(fn: str, status: int) -> None:
 
 
 def _ptr(x) -> Optional[int]:
+    """A device address: None, an int taken as is, or a contiguous CUDA
+    tensor's data pointer (a host tensor's address would send the kernels to
+    host memory, and a strided view would be read as if it were dense)."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    if not x.is_cuda:
+        raise ValueError("the library reads and writes device memory: pass CUDA tensors")
+    if not x.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
     return x.data_ptr()
 
 

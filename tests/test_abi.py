@@ -138,3 +138,14 @@ def test_rejected_calls_launch_nothing():
     assert _adamw([_table(rho_bits=3)]) == 4
     assert _call("fo_split", 16, 16, 16, -1, 8, None) == 3
     assert fo.fo_kernel_launch_count() == before
+
+
+def test_binding_rejects_host_and_strided_tensors():
+    """The binding refuses tensors the kernels would misread, before any call."""
+    import torch
+    x = torch.zeros(64)
+    with pytest.raises(ValueError, match="CUDA"):
+        fo.fo_split(x, torch.zeros(64, dtype=torch.int16), torch.zeros(64, dtype=torch.int8))
+    with pytest.raises(ValueError, match="CUDA"):
+        fo.row(x, None, None, None, None)
+    assert fo._ptr(None) is None and fo._ptr(1 << 20) == 1 << 20

@@ -189,3 +189,15 @@ def test_dequant_momentum_keeps_the_sign_of_zero():
     out = torch.empty(q.size, device="cuda")
     fo.fo_dequant_state(to_dev(q), to_dev(s), out, fo.FO_STATE_MOMENTUM)
     assert_exact(to_host(out), oracle.dequant_state(q, s, fo.FO_STATE_MOMENTUM), "signed zeros")
+
+
+def test_binding_rejects_strided_views():
+    """A strided view would be read as dense memory: the binding refuses it
+    before calling the library."""
+    x = torch.zeros(128, device="cuda")
+    tp = torch.empty(64, dtype=torch.int16, device="cuda")
+    rho = torch.empty(64, dtype=torch.int8, device="cuda")
+    with pytest.raises(ValueError, match="contiguous"):
+        fo.fo_split(x[::2], tp, rho)
+    fo.fo_split(x[:64], tp, rho)        # a contiguous slice is fine
+    torch.cuda.synchronize()
