@@ -43,7 +43,8 @@ def _step_and_compare(opt, st, g32, steps=2, hp=None):
     gb = wl.to_bf16_bits(g32)
     for t in range(1, steps + 1):
         ref = oracle_state_from_device(dev)
-        table = fo.table_of([dev], [to_dev(gb)])
+        gdev = to_dev(gb)                    # held until the step has run
+        table = fo.table_of([dev], [gdev])
         if opt == "adamw":
             oracle.adamw_step([ref], [gb], 1e-3, 0.9, 0.999, 1e-8, t)
             fo.fo_adamw_step(table, 1e-3, 0.9, 0.999, 1e-8, t)

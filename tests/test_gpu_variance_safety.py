@@ -47,8 +47,9 @@ def _parity(thetas, rho_bits, steps, seed, what):
         oracle.adamw_step(ref, grads, HP["lr"], HP["beta1"], HP["beta2"], HP["eps"], t, v_nonzero=True)
         oracle.adamw_step(plain, grads, HP["lr"], HP["beta1"], HP["beta2"], HP["eps"], t)
         moved += sum(int(np.count_nonzero(a.v_q != b.v_q)) for a, b in zip(ref, plain))
-        fo.fo_adamw_step(fo.table_of(dev, [to_dev(g) for g in grads]), HP["lr"], HP["beta1"], HP["beta2"],
-                         HP["eps"], t, v_nonzero=True)
+        gdev = [to_dev(g) for g in grads]    # held until the step has run
+        fo.fo_adamw_step(fo.table_of(dev, gdev), HP["lr"], HP["beta1"], HP["beta2"], HP["eps"], t,
+                         v_nonzero=True)
         torch.cuda.synchronize()
         for i, d in enumerate(dev):
             assert_state_matches(oracle_state_from_device(d), ref[i], f"{what} step {t} tensor {i}", total)
