@@ -42,9 +42,12 @@
  *
  * Memory and ownership: every array argument is DEVICE memory owned by the
  * caller (for example torch tensors' data pointers). The library allocates no
- * device or host memory and keeps no state between calls. Tables and
- * hyper-parameter structs are HOST memory, read only during the call (the
- * table is copied into kernel parameters before the call returns).
+ * device memory. Tables and hyper-parameter structs are HOST memory, read
+ * only during the call (the table is copied into kernel parameters before the
+ * call returns). To check a table for overlapping arrays, a step call sorts
+ * the table's address ranges in a per-thread host array (16 bytes per array
+ * of the largest table seen), kept until the thread exits; nothing else
+ * persists between calls.
  *
  * Layout: element arrays are contiguous, one element per entry; each array
  * must start on a 16-byte boundary. Scale arrays hold ceil(numel/32) FP16
@@ -52,13 +55,22 @@
  * tensor and the last group of a tensor may be partial.
  *
  * Streams and errors: all work is enqueued on `stream` (a cudaStream_t; NULL
- * is the legacy default stream) and the calls return without synchronizing.
- * Argument errors are detected on the host before anything is launched and
- * return a non-zero fo_status_t; launch errors return FO_ERR_CUDA. Faults
- * that happen later surface at the caller's next synchronization. Nothing is
- * thrown across the ABI. Calls on distinct streams over disjoint buffers are
- * independent and thread-safe. State buffers are updated in place; no two
- * arrays of one table row (the gradient and the state buffers) may overlap.
+ * is the legacy default stream) of the CURRENT device, and the calls return
+ * without synchronizing. Argument errors are detected on the host before
+ * anything is launched and return a non-zero fo_status_t. A CUDA error left
+ * pending by earlier, unrelated work is read (and so cleared) before the
+ * first launch and returned as FO_ERR_CUDA with nothing launched; a launch
+ * that fails returns FO_ERR_CUDA (fo_last_cuda_error gives the cudaError_t).
+ * A step table can need several launches (one per correction width and
+ * gradient type, and per 384 rows): if one of them fails, the launches
+ * before it stay enqueued, so the rows they cover are stepped and the others
+ * are not -- do not simply retry such a call. Faults that happen later
+ * surface at the caller's next synchronization. Nothing is thrown across the
+ * ABI. Calls on distinct streams over disjoint buffers are independent and
+ * thread-safe. State buffers are updated in place: an array that a call
+ * writes may share no byte with any other array of the call (FO_ERR_ALIAS),
+ * in the same table row or another; gradients are only read, so rows may
+ * share one gradient array.
  */
 #ifndef FO_H
 #define FO_H
@@ -78,7 +90,7 @@ typedef enum fo_status {
     FO_ERR_BAD_ARG = 4,          /* a flag or hyper-parameter is out of range   */
     FO_ERR_TOO_MANY_TENSORS = 5, /* ntensors exceeds FO_MAX_TENSORS             */
     FO_ERR_CUDA = 6,             /* a CUDA call failed (see fo_last_cuda_error) */
-    FO_ERR_ALIAS = 7             /* two arrays of one table row overlap         */
+    FO_ERR_ALIAS = 7             /* a written array overlaps another array      */
 } fo_status_t;
 
 /* Kind of optimizer state coded by fo_quant_state / fo_dequant_state. */
@@ -156,8 +168,9 @@ typedef struct fo_lion_hparams { double lr, beta1, beta2; } fo_lion_hparams_t;
  * fo_split -- weight splitting, section "权重复分裂" (Eq. 1-2): from FP32
  * weights theta_f32[n] write theta'[n] (BF16) and rho[n] (int8_t or int16_t
  * per rho_bits). Used to initialise the compressed weights.
- * Errors: FO_ERR_NULL, FO_ERR_MISALIGNED, FO_ERR_SIZE (n < 0),
- * FO_ERR_BAD_ARG (rho_bits not 8 or 16), FO_ERR_CUDA. n = 0 is a no-op.
+ * Errors: FO_ERR_NULL, FO_ERR_MISALIGNED, FO_ERR_SIZE (n < 0 or n > 2^46),
+ * FO_ERR_BAD_ARG (rho_bits not 8 or 16), FO_ERR_ALIAS (an output overlaps
+ * another array), FO_ERR_CUDA. n = 0 is a no-op.
  */
 fo_status_t fo_split(const float *theta_f32, uint16_t *theta_bf16, void *rho, int64_t n,
                      int32_t rho_bits, fo_stream_t stream);
@@ -175,7 +188,8 @@ fo_status_t fo_merge(const uint16_t *theta_bf16, const void *rho, float *theta_f
  * "带压缩扩展的优化器状态量化" (Algorithm 2 for m, Algorithm 3 for v):
  * x[n] (FP32; v must be >= 0) -> codes q[n] (int8_t for the momentum kinds,
  * uint8_t for the variance kinds) and scales[ceil(n/32)] (FP16).
- * Errors: FO_ERR_NULL, FO_ERR_MISALIGNED, FO_ERR_SIZE, FO_ERR_BAD_ARG (kind),
+ * Errors: FO_ERR_NULL, FO_ERR_MISALIGNED, FO_ERR_SIZE (n < 0 or n > 2^46),
+ * FO_ERR_BAD_ARG (kind), FO_ERR_ALIAS (an output overlaps another array),
  * FO_ERR_CUDA. n = 0 is a no-op.
  */
 fo_status_t fo_quant_state(const float *x, void *q, uint16_t *scales, int64_t n,

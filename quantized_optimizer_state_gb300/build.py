@@ -21,7 +21,11 @@ LIB = os.path.join(HERE, "libfo.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["fo_api.cu", "fo_step.cu", "fo_codecs.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
+# -Xcompiler -ffp-contract=off: the host code derives the per-step scalars in
+# double (1 - lr*wd and so on), which the contract defines as separately
+# rounded operations; gcc would contract them into fused multiply-adds on
+# aarch64.
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
               "-fmad=false", "-prec-div=true", "-prec-sqrt=true", "-ftz=false",
               "-Xptxas", "-warn-spills"]
 

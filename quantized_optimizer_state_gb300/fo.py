@@ -113,18 +113,38 @@ def _check(fn: str, status: int) -> None:
         raise FoError(fn, status, msg)
 
 
-def _ptr(x) -> Optional[int]:
-    """A device address: None, an int taken as is, or a contiguous CUDA
-    tensor's data pointer (a host tensor's address would send the kernels to
-    host memory, and a strided view would be read as if it were dense)."""
+def _current_device() -> int:
+    import torch
+    return torch.cuda.current_device()
+
+
+def _dtype_names(dtypes) -> str:
+    return " or ".join(str(d).replace("torch.", "") for d in dtypes)
+
+
+def _ptr(x, name: str = "tensor", dtypes=None, min_numel: Optional[int] = None) -> Optional[int]:
+    """A device address: None, an int taken as is, or the data pointer of a
+    contiguous CUDA tensor on the current device, of one of ``dtypes`` and with
+    at least ``min_numel`` elements. Every call launches on the current device,
+    so a host tensor, a strided view, a tensor of another device, a tensor of
+    the wrong element type or one too short for the call would make the
+    kernels read or write the wrong memory: each is refused here."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
     if not x.is_cuda:
-        raise ValueError("the library reads and writes device memory: pass CUDA tensors")
+        raise ValueError(f"{name}: the library reads and writes device memory: pass CUDA tensors")
     if not x.is_contiguous():
-        raise ValueError("tensors passed to the library must be contiguous")
+        raise ValueError(f"{name}: tensors passed to the library must be contiguous")
+    if dtypes is not None and x.dtype not in dtypes:
+        raise TypeError(f"{name} must be {_dtype_names(dtypes)}, not {str(x.dtype).replace('torch.', '')}")
+    if min_numel is not None and x.numel() < min_numel:
+        raise ValueError(f"{name} holds {x.numel()} elements; the call needs {min_numel}")
+    cur = _current_device()
+    if x.device.index != cur:
+        raise ValueError(f"{name} is on cuda:{x.device.index} but the current device is cuda:{cur}; "
+                         "the library launches on the current device (use torch.cuda.device)")
     return x.data_ptr()
 
 
@@ -136,6 +156,10 @@ def _stream(stream) -> Optional[int]:
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
+    dev = getattr(stream, "device", None)
+    if dev is not None and getattr(dev, "index", None) is not None and dev.index != _current_device():
+        raise ValueError(f"the stream belongs to cuda:{dev.index} but the current device is "
+                         f"cuda:{_current_device()}; the library launches on the current device")
     return stream.cuda_stream
 
 
@@ -145,56 +169,142 @@ def _numel(x, n):
     return int(x.numel())
 
 
+def _groups(n: int) -> int:
+    return (int(n) + GROUP - 1) // GROUP
+
+
+class _Dtypes:
+    """Element types the C ABI accepts for each kind of array (torch dtypes,
+    resolved on first use so that importing this module does not import torch)."""
+    _cache = None
+
+    @classmethod
+    def get(cls):
+        if cls._cache is None:
+            import torch
+            half_bits = (torch.int16, torch.bfloat16)          # BF16 bit patterns
+            scales = (torch.int16, torch.float16)              # FP16 bit patterns
+            if hasattr(torch, "uint16"):
+                half_bits += (torch.uint16,)
+                scales += (torch.uint16,)
+            cls._cache = {
+                "f32": (torch.float32,),
+                "bf16": half_bits,
+                "scale": scales,
+                "rho8": (torch.int8,),
+                "rho16": (torch.int16,),
+                "m_q": (torch.int8,),
+                "v_q": (torch.uint8,),
+            }
+        return cls._cache
+
+
+def _rho_dtypes(rho_bits: int):
+    return _Dtypes.get()["rho16" if int(rho_bits) == 16 else "rho8"]
+
+
+def _code_dtypes(kind: int):
+    variance = int(kind) in (FO_STATE_VARIANCE, FO_STATE_VARIANCE_LINEAR, FO_STATE_VARIANCE_NONZERO)
+    return _Dtypes.get()["v_q" if variance else "m_q"]
+
+
 # --- codecs ----------------------------------------------------------------
 
 def fo_split(theta_f32, theta_bf16, rho, rho_bits: int = 8, n: Optional[int] = None, stream=None):
-    _check("fo_split", lib().fo_split(_ptr(theta_f32), _ptr(theta_bf16), _ptr(rho),
-                                      _numel(theta_f32, n), rho_bits, _stream(stream)))
+    n = _numel(theta_f32, n)
+    d = _Dtypes.get()
+    _check("fo_split", lib().fo_split(_ptr(theta_f32, "theta_f32", d["f32"], n),
+                                      _ptr(theta_bf16, "theta_bf16", d["bf16"], n),
+                                      _ptr(rho, "rho", _rho_dtypes(rho_bits), n),
+                                      n, rho_bits, _stream(stream)))
 
 
 def fo_merge(theta_bf16, rho, theta_f32, rho_bits: int = 8, n: Optional[int] = None, stream=None):
-    _check("fo_merge", lib().fo_merge(_ptr(theta_bf16), _ptr(rho), _ptr(theta_f32),
-                                      _numel(theta_bf16, n), rho_bits, _stream(stream)))
+    n = _numel(theta_bf16, n)
+    d = _Dtypes.get()
+    _check("fo_merge", lib().fo_merge(_ptr(theta_bf16, "theta_bf16", d["bf16"], n),
+                                      _ptr(rho, "rho", _rho_dtypes(rho_bits), n),
+                                      _ptr(theta_f32, "theta_f32", d["f32"], n),
+                                      n, rho_bits, _stream(stream)))
 
 
 def fo_quant_state(x, q, scales, kind: int, n: Optional[int] = None, stream=None):
-    _check("fo_quant_state", lib().fo_quant_state(_ptr(x), _ptr(q), _ptr(scales), _numel(x, n),
+    n = _numel(x, n)
+    d = _Dtypes.get()
+    _check("fo_quant_state", lib().fo_quant_state(_ptr(x, "x", d["f32"], n), _ptr(q, "q", _code_dtypes(kind), n),
+                                                  _ptr(scales, "scales", d["scale"], _groups(n)), n,
                                                   kind, _stream(stream)))
 
 
 def fo_dequant_state(q, scales, x, kind: int, n: Optional[int] = None, stream=None):
-    _check("fo_dequant_state", lib().fo_dequant_state(_ptr(q), _ptr(scales), _ptr(x), _numel(q, n),
-                                                      kind, _stream(stream)))
+    n = _numel(q, n)
+    d = _Dtypes.get()
+    _check("fo_dequant_state", lib().fo_dequant_state(_ptr(q, "q", _code_dtypes(kind), n),
+                                                      _ptr(scales, "scales", d["scale"], _groups(n)),
+                                                      _ptr(x, "x", d["f32"], n), n, kind, _stream(stream)))
 
 
 # --- tables and fused steps ----------------------------------------------------
 
 class Table:
-    """A host array of ``fo_tensor_t`` rows, built once and reused across steps."""
+    """A host array of ``fo_tensor_t`` rows, built once and reused across steps.
+
+    The table holds a reference to every tensor its rows point into, so that
+    none of them can be freed (and its memory handed to another tensor by the
+    caching allocator) while the table is alive."""
 
     def __init__(self, rows: Sequence[FoTensor]):
         self.n = len(rows)
+        self.keep = [getattr(r, "keep", ()) for r in rows]
         self.rows = (FoTensor * max(1, self.n))(*rows)
 
     @property
     def ptr(self) -> int:
         return ctypes.addressof(self.rows)
 
+    def release(self) -> None:
+        """Drop the table's references to its tensors (the caller then keeps
+        them alive for as long as it uses the table). Work already enqueued is
+        unaffected: torch's allocator reuses freed memory in stream order."""
+        self.keep = []
+
 
 def _grad_dtype(grad, grad_dtype: Optional[int]) -> int:
-    """FP32 for a float32 tensor, else BF16 (bfloat16 or int16 bit patterns);
-    an explicit grad_dtype wins (needed for raw pointers)."""
-    if grad_dtype is not None:
-        return int(grad_dtype)
+    """fo_grad_dtype_t of a gradient: FP32 for a float32 tensor, BF16 for
+    bfloat16 (or int16 bit patterns); any other element type is refused rather
+    than read as BF16 words. For a raw address, grad_dtype says which
+    (BF16 when omitted)."""
     dt = getattr(grad, "dtype", None)
-    return GRAD_F32 if dt is not None and str(dt) == "torch.float32" else GRAD_BF16
+    if dt is None:
+        return GRAD_BF16 if grad_dtype is None else int(grad_dtype)
+    d = _Dtypes.get()
+    if dt in d["f32"]:
+        found = GRAD_F32
+    elif dt in d["bf16"]:
+        found = GRAD_BF16
+    else:
+        raise TypeError(f"grad must be bfloat16 (or int16 BF16 patterns) or float32, not "
+                        f"{str(dt).replace('torch.', '')}")
+    if grad_dtype is not None and int(grad_dtype) != found:
+        raise TypeError("grad_dtype does not match the gradient tensor's element type")
+    return found
 
 
 def row(theta, rho, m_q, m_scale, grad, v_q=None, v_scale=None, weight_decay: float = 0.0,
         rho_bits: int = 8, numel: Optional[int] = None, grad_dtype: Optional[int] = None) -> FoTensor:
-    return FoTensor(_ptr(theta), _ptr(rho), _ptr(m_q), _ptr(m_scale), _ptr(v_q), _ptr(v_scale),
-                    _ptr(grad), _numel(theta, numel), float(weight_decay), int(rho_bits),
-                    _grad_dtype(grad, grad_dtype))
+    """One ``fo_tensor_t``. Tensors are checked (device, contiguity, element
+    type, length) and kept alive by the row (and by any Table built from it)."""
+    n = _numel(theta, numel)
+    ng = _groups(n)
+    d = _Dtypes.get()
+    gdt = _grad_dtype(grad, grad_dtype)
+    r = FoTensor(_ptr(theta, "theta", d["bf16"], n), _ptr(rho, "rho", _rho_dtypes(rho_bits), n),
+                 _ptr(m_q, "m_q", d["m_q"], n), _ptr(m_scale, "m_scale", d["scale"], ng),
+                 _ptr(v_q, "v_q", d["v_q"], n), _ptr(v_scale, "v_scale", d["scale"], ng),
+                 _ptr(grad, "grad", d["f32"] if gdt == GRAD_F32 else d["bf16"], n), n,
+                 float(weight_decay), int(rho_bits), gdt)
+    r.keep = tuple(x for x in (theta, rho, m_q, m_scale, v_q, v_scale, grad) if x is not None and not isinstance(x, int))
+    return r
 
 
 def fo_adamw_step(table: Table, lr: float, beta1: float, beta2: float, eps: float, step: int,

@@ -12,8 +12,9 @@ kernel launch. Features from the page's practical advice:
 * per-group opt-out: ``rho_bits=16`` for a finer master weight, or
   ``compress=False`` to keep an FP32 master weight and FP32 moments updated by
   the standard PyTorch optimizer for that group;
-* gradient release: :meth:`attach_grad_release` steps each parameter as soon
-  as its gradient is accumulated and frees the gradient right away;
+* gradient release: :meth:`attach_grad_release` steps parameters during
+  backward as their gradients become ready (in buckets of a bounded size, one
+  fused call each) and frees each gradient once its step is enqueued;
 * compact checkpoints: :meth:`state_dict` holds theta' (through the model's
   parameters), rho, codes, scales and the step counters -- about 5 bytes per
   parameter for AdamW instead of 12;
@@ -154,27 +155,58 @@ class _FlashOptimizer(torch.optim.Optimizer):
         # number of steps share a call (a launch only touches its own device)
         by_key: Dict[tuple, List[torch.Tensor]] = {}
         for p in params:
-            st = self.state[p]
-            st["step"] = int(st["step"]) + 1
-            by_key.setdefault((st["step"], p.device.index), []).append(p)
+            by_key.setdefault((int(self.state[p]["step"]) + 1, p.device.index), []).append(p)
         for (t, dev), ps in by_key.items():
             grads = [self._grad_of(p) for p in ps]     # alive until the launch is enqueued
             with torch.cuda.device(dev):
-                self._launch(self._table(ps, grads, group), group, t)
+                table = self._table(ps, grads, group)
+                try:
+                    self._launch(table, group, t)
+                finally:
+                    # the cached table must not keep this step's gradients alive
+                    table.release()
+            # the step counters advance only once the call has succeeded, so a
+            # refused call (fo.FoError) leaves them as they were
+            for p in ps:
+                self.state[p]["step"] = t
 
     def _launch(self, table: fo.Table, group: Dict, t: int) -> None:
         raise NotImplementedError
 
     # -- gradient release ---------------------------------------------------
 
-    def attach_grad_release(self, params: Optional[Iterable[torch.Tensor]] = None) -> List:
-        """Step each compressed parameter as soon as its gradient has been
-        accumulated and drop the gradient, so that at most one gradient per
-        parameter is alive during backward (no gradient accumulation across
-        backward passes). Returns the hook handles."""
+    def attach_grad_release(self, params: Optional[Iterable[torch.Tensor]] = None,
+                            bucket_numel: int = 1 << 24) -> List:
+        """Step compressed parameters during backward, as their gradients
+        become ready, and free each gradient once its step is enqueued (no
+        gradient accumulation across backward passes).
+
+        Parameters whose gradients are ready wait in a bucket per parameter
+        group; the bucket is stepped in one fused call once it holds
+        ``bucket_numel`` elements, and whatever is left is stepped at the end
+        of the backward pass. At most about ``bucket_numel`` elements of
+        gradient per group are therefore alive beyond the one autograd is
+        producing; ``bucket_numel=0`` steps each parameter on its own. Returns
+        the hook handles."""
         handles = []
         groups = {id(p): g for g in self.param_groups for p in g["params"]}
         wanted = None if params is None else {id(p) for p in params}
+        pending: Dict[int, list] = {}        # id(group) -> [group, params, numel]
+        queued = [False]
+
+        def flush(gid: int) -> None:
+            group, ps, _ = pending.pop(gid)
+            with torch.no_grad():
+                self._step_params(ps, group)
+            for q in ps:
+                q.grad = None
+
+        def flush_all() -> None:
+            queued[0] = False
+            for gid in list(pending):
+                flush(gid)
+
+        self._release_flush = flush_all
         for p_id, group in groups.items():
             if not group["compress"]:
                 continue
@@ -183,12 +215,25 @@ class _FlashOptimizer(torch.optim.Optimizer):
                     continue
 
                 def hook(param, group=group):
-                    with torch.no_grad():
-                        self._step_params([param], group)
-                    param.grad = None
+                    entry = pending.setdefault(id(group), [group, [], 0])
+                    entry[1].append(param)
+                    entry[2] += param.numel()
+                    if entry[2] >= bucket_numel:
+                        flush(id(group))
+                    elif not queued[0]:
+                        # the rest of the bucket is stepped when this backward pass ends
+                        torch.autograd.Variable._execution_engine.queue_callback(flush_all)
+                        queued[0] = True
 
                 handles.append(p.register_post_accumulate_grad_hook(hook))
         return handles
+
+    def flush_grad_release(self) -> None:
+        """Step the parameters still waiting in a gradient-release bucket (for
+        a backward pass that ended early, for example through an exception)."""
+        f = getattr(self, "_release_flush", None)
+        if f is not None:
+            f()
 
     # -- checkpoints ----------------------------------------------------------
 

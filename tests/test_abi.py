@@ -149,3 +149,106 @@ def test_binding_rejects_host_and_strided_tensors():
     with pytest.raises(ValueError, match="CUDA"):
         fo.row(x, None, None, None, None)
     assert fo._ptr(None) is None and fo._ptr(1 << 20) == 1 << 20
+
+
+def test_rows_of_one_table_may_not_share_written_memory():
+    """Every array a step writes must be disjoint from every other array of the
+    table, in its own row or another (one launch would race; two launches
+    would step the same state twice)."""
+    MB = 1 << 20
+    second = dict(theta=(1 << 26), rho=(1 << 26) + MB, m_q=(1 << 26) + 2 * MB, m_scale=(1 << 26) + 3 * MB,
+                  v_q=(1 << 26) + 4 * MB, v_scale=(1 << 26) + 5 * MB, grad=(1 << 26) + 6 * MB)
+    assert _adamw([_table(), _table()]) == 7                                   # the same row twice
+    assert _adamw([_table(), _table(**dict(second, theta=(1 << 24) + 64))]) == 7   # theta' inside theta'
+    assert _adamw([_table(), _table(**dict(second, grad=(1 << 24) + (2 << 20)))]) == 7  # grad over m codes
+    assert _adamw([_table(), _table(**dict(second, v_scale=(1 << 24) + (5 << 20) + 6))]) == 7   # last 2 bytes
+    assert _adamw([_table(numel=0), _table(numel=0)]) == 0                     # empty rows hold nothing
+    # rows of different launches (correction widths) are checked too
+    assert _adamw([_table(), _table(**dict(second, rho_bits=16, m_q=(1 << 24) + 32))]) == 7
+    sgd = fo.SGDHparams(0.1, 0.9)
+    two = (fo.FoTensor * 2)(_table(v_q=None, v_scale=None),
+                            _table(**dict(second, v_q=None, v_scale=None, m_scale=(1 << 24) + (3 << 20) + 2)))
+    assert _call("fo_sgd_step", ctypes.addressof(two), 2, ctypes.addressof(sgd), None) == 7
+
+
+def test_codec_outputs_may_not_overlap_their_inputs():
+    A = 1 << 20
+    assert _call("fo_split", A, A + 16, A + 4096, 10, 8, None) == 7           # theta' inside the FP32 input
+    assert _call("fo_split", A, A + 4096, A + 4096 + 16, 10, 8, None) == 7    # rho inside theta'
+    assert _call("fo_merge", A, A + 4096, A + 16, 10, 8, None) == 7           # output over theta'
+    assert _call("fo_quant_state", A, A + 4096, A + 4096 + 4, 64, 0, None) == 7  # scales inside the codes
+    assert _call("fo_dequant_state", A, A + 4096, A + 32, 64, 1, None) == 7   # output over the codes
+    assert _call("fo_split", A, A, A, (1 << 46) + 1, 8, None) == 3            # size bound
+
+
+class _FakeCuda:
+    """Stands in for a CUDA tensor in binding checks that run before any call."""
+
+    def __init__(self, dtype, n, dev=0, addr=1 << 20):
+        import types
+        self.dtype, self._n, self._addr = dtype, n, addr
+        self.device = types.SimpleNamespace(index=dev)
+        self.is_cuda = True
+
+    def is_contiguous(self):
+        return True
+
+    def numel(self):
+        return self._n
+
+    def data_ptr(self):
+        return self._addr
+
+
+def test_binding_rejects_wrong_device_dtype_and_length(monkeypatch):
+    import types
+    import torch
+    monkeypatch.setattr(fo, "_current_device", lambda: 0)
+    F = _FakeCuda
+    n = 100
+    ok = dict(theta=F(torch.int16, n), rho=F(torch.int8, n), m_q=F(torch.int8, n), m_scale=F(torch.int16, 4),
+              grad=F(torch.bfloat16, n), v_q=F(torch.uint8, n), v_scale=F(torch.float16, 4))
+    r = fo.row(**ok)
+    assert r.numel == n and r.grad_dtype == fo.GRAD_BF16 and len(r.keep) == 7
+    assert fo.row(**dict(ok, grad=F(torch.float32, n))).grad_dtype == fo.GRAD_F32
+    with pytest.raises(ValueError, match="cuda:1"):
+        fo.row(**dict(ok, m_q=F(torch.int8, n, dev=1)))                 # another device's tensor
+    for name, bad in [("theta", F(torch.float32, n)), ("rho", F(torch.int16, n)), ("m_q", F(torch.uint8, n)),
+                      ("v_q", F(torch.int8, n)), ("m_scale", F(torch.float32, 4)),
+                      ("grad", F(torch.float16, n)), ("grad", F(torch.float64, n)), ("grad", F(torch.int8, n))]:
+        with pytest.raises(TypeError, match=name):
+            fo.row(**dict(ok, **{name: bad}))
+    with pytest.raises(TypeError):
+        fo.row(**ok, grad_dtype=fo.GRAD_F32)                            # contradicts the tensor's type
+    with pytest.raises(TypeError, match="rho"):
+        fo.row(**dict(ok, rho=F(torch.int8, n)), rho_bits=16)
+    with pytest.raises(ValueError, match="needs 4"):
+        fo.row(**dict(ok, v_scale=F(torch.int16, 3)))                   # too few scales
+    with pytest.raises(ValueError, match="needs 100"):
+        fo.row(**dict(ok, grad=F(torch.bfloat16, 99)))
+    with pytest.raises(TypeError, match="q"):
+        fo.fo_quant_state(F(torch.float32, n), F(torch.int8, n), F(torch.int16, 4), fo.FO_STATE_VARIANCE)
+    with pytest.raises(TypeError, match="x"):
+        fo.fo_dequant_state(F(torch.int8, n), F(torch.int16, 4), F(torch.float16, n), fo.FO_STATE_MOMENTUM)
+    with pytest.raises(ValueError, match="needs"):
+        fo.fo_split(F(torch.float32, n), F(torch.int16, n - 1), F(torch.int8, n))
+    stream = types.SimpleNamespace(device=types.SimpleNamespace(index=2), cuda_stream=0)
+    with pytest.raises(ValueError, match="stream"):
+        fo._stream(stream)
+
+
+def test_table_keeps_its_tensors_alive(monkeypatch):
+    import gc
+    import weakref
+    import torch
+    monkeypatch.setattr(fo, "_current_device", lambda: 0)
+    F = _FakeCuda
+    g = F(torch.bfloat16, 64)
+    ref = weakref.ref(g)
+    t = fo.Table([fo.row(F(torch.int16, 64), F(torch.int8, 64), F(torch.int8, 64), F(torch.int16, 2), g)])
+    del g
+    gc.collect()
+    assert ref() is not None                # the table holds the gradient it points into
+    t.release()
+    gc.collect()
+    assert ref() is None

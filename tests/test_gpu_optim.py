@@ -182,13 +182,18 @@ def test_cached_table_with_in_place_grads_and_changed_weight_decay():
     assert len(opt._tables) == 1
 
 
-@pytest.mark.skipif(not hasattr(torch.Tensor, "grad_dtype"), reason="this torch has no Tensor.grad_dtype")
+@pytest.mark.parametrize("route", ["grad_dtype", "step_params"])
 @pytest.mark.parametrize("kind", ["adamw", "lion"])
-def test_fp32_gradients_reach_the_step_unrounded(kind):
-    """With grad_dtype float32, autograd accumulates FP32 gradients for the
-    BF16 parameters; the step must read them as FP32 (the oracle's FP32
-    gradient path), not rounded to BF16. Negative control: the oracle fed
-    the same gradients rounded to BF16 ends in another state."""
+def test_fp32_gradients_reach_the_step_unrounded(kind, route):
+    """FP32 gradients of BF16 parameters must reach the step as FP32 (the
+    oracle's FP32-gradient path), not rounded to BF16. Route "grad_dtype":
+    autograd accumulates them with Tensor.grad_dtype = float32 (PyTorch
+    versions that have it). Route "step_params": the same gradients handed to
+    the optimizer's stepping code directly, so the FP32 path runs on any
+    PyTorch. Negative control: the oracle fed the same gradients rounded to
+    BF16 ends in another state."""
+    if route == "grad_dtype" and not hasattr(torch.Tensor, "grad_dtype"):
+        pytest.skip("this torch has no Tensor.grad_dtype")
     params = _params(11)
     master0 = [p.detach().clone() for p in params]
     if kind == "adamw":
@@ -197,8 +202,12 @@ def test_fp32_gradients_reach_the_step_unrounded(kind):
         opt = optim.FlashLion(params, lr=1e-4, weight_decay=0.01)
     ref = _oracle_states(master0, 8, kind == "adamw", 0.01)
     rounded = [r.copy() for r in ref]
-    for p in params:
-        p.grad_dtype = torch.float32
+    fp32_grads = {}
+    if route == "grad_dtype":
+        for p in params:
+            p.grad_dtype = torch.float32
+    else:
+        opt._grad_of = lambda p: fp32_grads[id(p)]
     rng = np.random.default_rng(12)
 
     def oracle_step(states, grads, t):
@@ -210,12 +219,77 @@ def test_fp32_gradients_reach_the_step_unrounded(kind):
     for t in range(1, 4):
         grads = [(rng.standard_t(3, p.numel()) * 1e-3).astype(np.float32) for p in params]
         for p, g in zip(params, grads):
-            p.grad = torch.from_numpy(g).cuda().view(p.shape)
-            assert p.grad.dtype == torch.float32
-        opt.step()
+            if route == "grad_dtype":
+                p.grad = torch.from_numpy(g).cuda().view(p.shape)
+                assert p.grad.dtype == torch.float32
+            else:
+                fp32_grads[id(p)] = torch.from_numpy(g).cuda()
+        if route == "grad_dtype":
+            opt.step()
+        else:
+            opt._step_params(params, opt.param_groups[0])
         oracle_step(ref, grads, t)
         oracle_step(rounded, [wl.to_bf16_bits(g) for g in grads], t)
         torch.cuda.synchronize()
         for p, r in zip(params, ref):
             assert_state_matches(_device_view(opt, p), r, f"{kind} fp32 grad step {t}")
     assert any(not np.array_equal(_device_view(opt, p).m_q, r.m_q) for p, r in zip(params, rounded))
+
+
+@pytest.mark.parametrize("bucket", [0, 3000, 1 << 30])
+def test_gradient_release_buckets_match_plain_step(bucket):
+    """Release with every parameter stepped on its own (bucket 0), in buckets
+    that fill during backward (3000 elements) and in one bucket stepped when
+    backward ends: all equal the plain step bit for bit, and every gradient
+    is freed."""
+    a, b = _model(13), _model(13)
+    oa = optim.FlashAdamW(a.parameters(), lr=1e-3)
+    ob = optim.FlashAdamW(b.parameters(), lr=1e-3)
+    _train(a, oa, 3, release=False)
+    ob.attach_grad_release(bucket_numel=bucket)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    for _ in range(3):
+        x = torch.randn(64, 48, device="cuda", generator=g).to(torch.bfloat16)
+        b(x).float().square().mean().backward()
+        assert all(p.grad is None for p in b.parameters())
+    torch.cuda.synchronize()
+    for pa, pb in zip(a.parameters(), b.parameters()):
+        assert torch.equal(pa.data, pb.data)
+        assert ob.state[pb]["step"] == 3
+        for k in ("rho", "m_q", "m_scale", "v_q", "v_scale"):
+            assert torch.equal(oa.state[pa][k], ob.state[pb][k])
+
+
+def test_failed_call_leaves_step_counters_unchanged():
+    from quantized_optimizer_state_gb300 import fo
+    params = _params(21)
+    opt = optim.FlashAdamW(params, lr=1e-3)
+    for p in params:
+        p.grad = torch.zeros(p.shape, dtype=torch.bfloat16, device="cuda")
+
+    def refuse(table, group, t):
+        raise fo.FoError("fo_adamw_step", 4, "refused")
+
+    opt._launch = refuse
+    with pytest.raises(fo.FoError):
+        opt.step()
+    assert all(opt.state[p]["step"] == 0 for p in params)
+    del opt._launch
+    opt.step()
+    assert all(opt.state[p]["step"] == 1 for p in params)
+
+
+def test_cached_table_does_not_keep_gradients_alive():
+    """The optimizer reuses its tables across steps, but a table must not hold
+    the step's gradients: freeing them after the step frees their memory."""
+    import gc
+    import weakref
+    params = _params(22)
+    opt = optim.FlashAdamW(params, lr=1e-3)
+    for p in params:
+        p.grad = torch.zeros(p.shape, dtype=torch.bfloat16, device="cuda")
+    refs = [weakref.ref(p.grad) for p in params]
+    opt.step()
+    opt.zero_grad(set_to_none=True)
+    gc.collect()
+    assert all(r() is None for r in refs)
