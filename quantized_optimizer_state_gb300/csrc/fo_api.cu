@@ -1,9 +1,11 @@
 // fo_api.cu -- the C ABI declared in include/fo.h: argument validation,
 // per-step scalar derivation and kernel launches. No entry point allocates
-// memory, synchronizes, or falls back to the CPU.
+// device memory, synchronizes, or falls back to the CPU.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <vector>
 
 #include "fo.h"
 #include "fo_internal.h"
@@ -69,14 +71,6 @@ double pow_by_squaring(double b, int64_t t)
     return r;
 }
 
-bool overlaps(const void *a, int64_t abytes, const void *b, int64_t bbytes)
-{
-    if (!a || !b || abytes <= 0 || bbytes <= 0)
-        return false;
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
-    return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
-}
-
 fo_status_t check_row(const fo_tensor_t &t, bool with_v)
 {
     if (t.numel < 0)
@@ -96,18 +90,69 @@ fo_status_t check_row(const fo_tensor_t &t, bool with_v)
         return FO_ERR_MISALIGNED;
     if ((reinterpret_cast<uintptr_t>(t.m_scale) & 1u) || (with_v && (reinterpret_cast<uintptr_t>(t.v_scale) & 1u)))
         return FO_ERR_MISALIGNED;
-    // no two arrays of the row may share a byte: the step reads each one and
-    // writes the state arrays in place
-    const int64_t n = t.numel, ng = (n + 31) / 32;
-    const void *ptr[7] = {t.grad, t.theta, t.rho, t.m_q, t.m_scale, t.v_q, t.v_scale};
-    const int64_t bytes[7] = {(t.grad_dtype == FO_GRAD_F32 ? 4 : 2) * n, 2 * n, n * (t.rho_bits / 8), n, 2 * ng,
-                              n, 2 * ng};
-    const int count = with_v ? 7 : 5;
-    for (int a = 0; a < count; ++a)
-        for (int b = a + 1; b < count; ++b)
-            if (overlaps(ptr[a], bytes[a], ptr[b], bytes[b]))
-                return FO_ERR_ALIAS;
     return FO_OK;
+}
+
+// One array of a table row: bytes [lo, hi), and whether the step writes it.
+struct Span {
+    uintptr_t lo, hi;
+    bool written;
+};
+
+// No array that a step writes may share a byte with any other array of the
+// table (in the same row or another): rows updated by one launch would race,
+// and rows of different launches would be stepped twice. Gradients are only
+// read, so several rows may share one. The spans are sorted by start address
+// (O(n log n)); a per-thread scratch array holds them between calls.
+fo_status_t check_disjoint(const fo_tensor_t *table, int32_t ntensors, bool with_v)
+{
+    static thread_local std::vector<Span> spans;
+    try {
+        spans.clear();
+        spans.reserve((size_t)ntensors * (with_v ? 7 : 5));
+    } catch (...) {
+        return FO_ERR_SIZE;
+    }
+    for (int32_t i = 0; i < ntensors; ++i) {
+        const fo_tensor_t &t = table[i];
+        if (t.numel <= 0)
+            continue;
+        const int64_t n = t.numel, ng = (n + 31) / 32;
+        const void *ptr[7] = {t.grad, t.theta, t.rho, t.m_q, t.m_scale, t.v_q, t.v_scale};
+        const int64_t bytes[7] = {(t.grad_dtype == FO_GRAD_F32 ? 4 : 2) * n, 2 * n, n * (t.rho_bits / 8), n,
+                                  2 * ng, n, 2 * ng};
+        const int count = with_v ? 7 : 5;
+        for (int a = 0; a < count; ++a) {
+            const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr[a]);
+            spans.push_back(Span{lo, lo + (uintptr_t)bytes[a], a != 0});
+        }
+    }
+    std::sort(spans.begin(), spans.end(), [](const Span &x, const Span &y) { return x.lo < y.lo; });
+    // a span overlaps an earlier-starting one exactly when it starts below that
+    // one's end: track the furthest end among written spans and among all
+    uintptr_t end_written = 0, end_any = 0;
+    for (const Span &sp : spans) {
+        if (sp.lo < end_written || (sp.written && sp.lo < end_any))
+            return FO_ERR_ALIAS;
+        end_any = std::max(end_any, sp.hi);
+        if (sp.written)
+            end_written = std::max(end_written, sp.hi);
+    }
+    return FO_OK;
+}
+
+// A CUDA error left pending by earlier work (a non-sticky launch error that
+// nobody has read yet) would be reported by the first cudaGetLastError after
+// this call's own launch, and the call would look failed after part of its
+// work was enqueued. So it is read (and cleared) before anything is launched,
+// and reported as this call's FO_ERR_CUDA, with nothing launched.
+fo_status_t pending_error()
+{
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess)
+        return FO_OK;
+    fo::t_last_cuda_error = (int)e;
+    return FO_ERR_CUDA;
 }
 
 // Per-row scalar: decay (AdamW, Lion) or weight decay (SGD), rounded once to FP32.
@@ -125,11 +170,20 @@ fo_status_t run_table(Opt opt, const fo_tensor_t *table, int32_t ntensors, const
     if (!table)
         return FO_ERR_NULL;
     const bool with_v = opt == Opt::kAdamW;
+    bool any_work = false;
     for (int32_t i = 0; i < ntensors; ++i) {
         const fo_status_t st = check_row(table[i], with_v);
         if (st != FO_OK)
             return st;
+        any_work = any_work || table[i].numel > 0;
     }
+    if (!any_work)
+        return FO_OK;
+    fo_status_t st0 = check_disjoint(table, ntensors, with_v);
+    if (st0 == FO_OK)
+        st0 = pending_error();
+    if (st0 != FO_OK)
+        return st0;
 
     // Pack rows into launches of one correction width and one gradient type,
     // at most kRowsPerLaunch rows and 2^31-1 tiles each (a kernel is
@@ -196,6 +250,45 @@ fo_status_t run_table(Opt opt, const fo_tensor_t *table, int32_t ntensors, const
 
 float decay_coef(double lr, double wd) { return (float)(1.0 - lr * wd); }
 
+// The fast path's range for a checked operand x: x = 0 or lo <= |x| <= hi,
+// stored as the FP32 values just below lo and hi (see StepScalars).
+void set_range(fo::StepScalars &s, float lo, float hi)
+{
+    s.lo = std::nextafter(lo, 0.0f);
+    s.hi = std::nextafter(hi, 0.0f);
+}
+
+// AdamW's packed fast path (fo_step.cu, pair_fast) divides and takes square
+// roots with sequences validated for operands in [2^-100, 2^100] (and zero
+// numerators). With the per-element check that the gradient g is 0 or
+// T <= |g| <= 2^24, these conditions keep every operand inside:
+//  - eps in [2^-40, 2^20] and 1/sqrt(bc2) <= 2^8: den in [2^-40, 2^33];
+//  - b1, b2 zero or at least 2^-16 and 1-b1, 1-b2 at least 2^-24: a non-zero
+//    v is at least 2^-99 and a non-zero m at least 2^-94 (a decoded non-zero
+//    momentum is at least 2^-32 and its second moment 2^-64; a cancellation
+//    in b1*m + (1-b1)*g leaves a multiple of the operands' finest ulp);
+//  - T is the smallest power of two with (1-b1)*T >= 2^-96 and
+//    (1-b2)*T^2 >= 2^-98, so that a gradient alone gives the same bounds;
+//  - lr/bc1 zero or at least 2^-80: its 2^-32 scaling stays exact;
+//  - per thread, the largest sqrt(v) at most 2^40, which bounds |g| by 2^52
+//    and |m| by 2^53 (v >= (1-b2)*g^2).
+// Then m' = 2^32 m and m'/den lie in [2^-100, 2^100] or are zero (a large
+// gradient also makes den large), and phi_m's quotient too. Calls outside
+// these conditions take the IEEE path throughout.
+void adamw_fast_ranges(fo::StepScalars &s)
+{
+    const float b1 = s.a[0], b2 = s.a[1], c1 = s.a[2], c2 = s.a[3], step = -s.a[5];
+    bool fast = s.a[4] >= 0x1p-40f && s.a[4] <= 0x1p20f && s.a[6] <= 0x1p8f;
+    fast = fast && (b1 == 0.0f || b1 >= 0x1p-16f) && (b2 == 0.0f || b2 >= 0x1p-16f);
+    fast = fast && c1 >= 0x1p-24f && c2 >= 0x1p-24f;
+    fast = fast && (step == 0.0f || step >= 0x1p-80f);
+    double t = 0x1p-100;
+    while (t < 0x1p-30 && !((double)c1 * t >= 0x1p-96 && (double)c2 * t * t >= 0x1p-98))
+        t *= 2.0;
+    s.fast = fast ? 1 : 0;
+    set_range(s, (float)t, __builtin_inff());   // the upper bound is checked through sqrt(v)
+}
+
 // Both lanes of a packed FP32 pair set to x.
 unsigned long long lanes(float x)
 {
@@ -219,9 +312,29 @@ fo_status_t check_codec(const void *a, const void *b, const void *c, int64_t n)
         return FO_ERR_SIZE;
     if (n == 0)
         return FO_OK;
+    if (n > ((int64_t)1 << 46))
+        return FO_ERR_SIZE;
     if (!a || !b || !c)
         return FO_ERR_NULL;
     return FO_OK;
+}
+
+bool overlap(const void *a, int64_t abytes, const void *b, int64_t bbytes)
+{
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
+}
+
+// A codec reads one or two arrays and writes the others: the written arrays
+// may share no byte with any other array of the call. Arrays 0..nin-1 are
+// read, the rest written.
+bool codec_aliases(int nin, const void *const *ptr, const int64_t *bytes, int count)
+{
+    for (int a = 0; a < count; ++a)
+        for (int b = a + 1; b < count; ++b)
+            if ((a >= nin || b >= nin) && overlap(ptr[a], bytes[a], ptr[b], bytes[b]))
+                return true;
+    return false;
 }
 
 }  // namespace
@@ -238,6 +351,14 @@ fo_status_t fo_split(const float *theta_f32, uint16_t *theta_bf16, void *rho, in
         return FO_ERR_BAD_ARG;
     if (!aligned16(theta_f32) || !aligned16(theta_bf16) || !aligned16(rho))
         return FO_ERR_MISALIGNED;
+    {
+        const void *ptr[3] = {theta_f32, theta_bf16, rho};
+        const int64_t bytes[3] = {4 * n, 2 * n, n * (rho_bits / 8)};
+        if (codec_aliases(1, ptr, bytes, 3))
+            return FO_ERR_ALIAS;
+    }
+    if ((st = pending_error()) != FO_OK)
+        return st;
     return cuda_status(fo::launch_split(theta_f32, theta_bf16, rho, n, rho_bits, static_cast<cudaStream_t>(stream)));
 }
 
@@ -251,6 +372,14 @@ fo_status_t fo_merge(const uint16_t *theta_bf16, const void *rho, float *theta_f
         return FO_ERR_BAD_ARG;
     if (!aligned16(theta_f32) || !aligned16(theta_bf16) || !aligned16(rho))
         return FO_ERR_MISALIGNED;
+    {
+        const void *ptr[3] = {theta_bf16, rho, theta_f32};
+        const int64_t bytes[3] = {2 * n, n * (rho_bits / 8), 4 * n};
+        if (codec_aliases(2, ptr, bytes, 3))
+            return FO_ERR_ALIAS;
+    }
+    if ((st = pending_error()) != FO_OK)
+        return st;
     return cuda_status(fo::launch_merge(theta_bf16, rho, theta_f32, n, rho_bits, static_cast<cudaStream_t>(stream)));
 }
 
@@ -264,6 +393,14 @@ fo_status_t fo_quant_state(const float *x, void *q, uint16_t *scales, int64_t n,
         return FO_ERR_BAD_ARG;
     if (!aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(scales) & 1u))
         return FO_ERR_MISALIGNED;
+    {
+        const void *ptr[3] = {x, q, scales};
+        const int64_t bytes[3] = {4 * n, n, 2 * ((n + 31) / 32)};
+        if (codec_aliases(1, ptr, bytes, 3))
+            return FO_ERR_ALIAS;
+    }
+    if ((st = pending_error()) != FO_OK)
+        return st;
     return cuda_status(fo::launch_quant(x, q, scales, n, (int)kind, static_cast<cudaStream_t>(stream)));
 }
 
@@ -277,6 +414,14 @@ fo_status_t fo_dequant_state(const void *q, const uint16_t *scales, float *x, in
         return FO_ERR_BAD_ARG;
     if (!aligned16(x) || !aligned16(q) || (reinterpret_cast<uintptr_t>(scales) & 1u))
         return FO_ERR_MISALIGNED;
+    {
+        const void *ptr[3] = {q, scales, x};
+        const int64_t bytes[3] = {n, 2 * ((n + 31) / 32), 4 * n};
+        if (codec_aliases(2, ptr, bytes, 3))
+            return FO_ERR_ALIAS;
+    }
+    if ((st = pending_error()) != FO_OK)
+        return st;
     return cuda_status(fo::launch_dequant(q, scales, x, n, (int)kind, static_cast<cudaStream_t>(stream)));
 }
 
@@ -301,17 +446,15 @@ fo_status_t fo_adamw_step(const fo_tensor_t *table, int32_t ntensors, const fo_a
     s.a[4] = (float)hp->eps;
     s.a[5] = -(float)(hp->lr / bc1);
     s.a[6] = (float)(1.0 / std::sqrt(bc2));
-    s.p[0] = lanes(s.a[0]);
+    // the packed fast path carries m' = 2^32 m (exact scalings of the constants)
+    s.p[0] = lanes(s.a[0] * 0x1p32f);
     s.p[1] = lanes(-s.a[1]);
-    s.p[2] = lanes(s.a[2]);
+    s.p[2] = lanes(s.a[2] * 0x1p32f);
     s.p[3] = lanes(-s.a[3]);
     s.p[4] = lanes(s.a[6]);
     s.p[5] = lanes(-s.a[4]);
-    s.p[6] = lanes(s.a[5]);
-    // validated operand ranges of the packed division/square root: den = sqrt(v)
-    // /sqrt(bc2) + eps stays in [2^-40, 2^40] when these hold (|g| <= 2^24 is
-    // checked per element)
-    s.fast = (s.a[4] >= 0x1p-40f && s.a[4] <= 0x1p20f && s.a[6] <= 0x1p8f) ? 1 : 0;
+    s.p[6] = lanes(s.a[5] * 0x1p-32f);
+    adamw_fast_ranges(s);
     s.v_nonzero = (hp->flags & FO_ADAMW_V_NONZERO) ? 1 : 0;
     return run_table(Opt::kAdamW, table, ntensors, s, hp->lr, decay_coef, stream);
 }
@@ -329,6 +472,7 @@ fo_status_t fo_sgd_step(const fo_tensor_t *table, int32_t ntensors, const fo_sgd
     s.p[0] = lanes(s.a[0]);
     s.p[1] = lanes(s.a[1]);
     s.fast = 1;
+    set_range(s, 0x1p-100f, 0x1p100f);   // the new momentum: phi_m's validated range
     return run_table(Opt::kSgd, table, ntensors, s, hp->lr, wd_coef, stream);
 }
 
@@ -349,6 +493,7 @@ fo_status_t fo_lion_step(const fo_tensor_t *table, int32_t ntensors, const fo_li
     for (int i = 0; i < 5; ++i)
         s.p[i] = lanes(s.a[i]);
     s.fast = 1;
+    set_range(s, 0x1p-100f, 0x1p100f);   // the new momentum: phi_m's validated range
     return run_table(Opt::kLion, table, ntensors, s, hp->lr, decay_coef, stream);
 }
 
@@ -362,7 +507,7 @@ const char *fo_status_string(fo_status_t status)
     case FO_ERR_BAD_ARG: return "FO_ERR_BAD_ARG: a flag or hyper-parameter is out of range";
     case FO_ERR_TOO_MANY_TENSORS: return "FO_ERR_TOO_MANY_TENSORS: ntensors exceeds FO_MAX_TENSORS";
     case FO_ERR_CUDA: return "FO_ERR_CUDA: a CUDA call failed";
-    case FO_ERR_ALIAS: return "FO_ERR_ALIAS: two arrays of one table row overlap";
+    case FO_ERR_ALIAS: return "FO_ERR_ALIAS: an array the call writes overlaps another array of the call";
     }
     return "unknown fo_status_t";
 }

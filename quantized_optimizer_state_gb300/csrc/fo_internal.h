@@ -53,16 +53,21 @@ static_assert(sizeof(StepRow) == 72, "StepRow layout");
 //  SGD:   a = {momentum, -lr}
 //  Lion:  a = {beta1, beta2, 1-beta1, 1-beta2, -lr}
 // and the same values as lane pairs for the packed fast path (p), with the
-// signs that path needs:
-//  AdamW: p = {b1, -b2, 1-b1, -(1-b2), 1/sqrt(bc2), -eps, -lr/bc1}
+// signs and scalings that path needs (AdamW carries m scaled by 2^32):
+//  AdamW: p = {2^32 b1, -b2, 2^32 (1-b1), -(1-b2), 1/sqrt(bc2), -eps, -2^-32 lr/bc1}
 //  SGD:   p = {momentum, -lr}
 //  Lion:  p = {b1, b2, 1-b1, 1-b2, -lr}
 // fast = 1 when the call's hyper-parameters keep the fast path's operands in
-// its validated ranges (AdamW: eps in [2^-40, 2^20], 1/sqrt(bc2) <= 2^8).
+// its validated ranges (conditions in fo_api.cu).
+// lo, hi: the fast path's range for its checked operand x (AdamW: the
+// gradient; SGD, Lion: the new momentum): x = 0 or lo' <= |x| <= hi', given
+// as the FP32 values just below lo' and hi' (the guard compares the float
+// below |x|, see Guard in fo_step.cu).
 // v_nonzero (AdamW): requantize v with no code 0 in a group with a non-zero scale.
 struct StepScalars {
     float a[8];
     unsigned long long p[8];
+    float lo, hi;
     int32_t fast;
     int32_t v_nonzero;
 };

@@ -64,6 +64,14 @@ __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c)
 
 __device__ __forceinline__ f2 splat(float x) { return pk(x, x); }
 
+// max(a, b, c) with NaN propagated (a NaN operand gives NaN), in one instruction.
+__device__ __forceinline__ float max3_nan(float a, float b, float c)
+{
+    float d;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float rcp_approx(float x)
 {
     float y;
@@ -104,11 +112,15 @@ __device__ __forceinline__ f2 div2(f2 a, f2 nb)
 // -RN(sqrt(v)) in both lanes, given nv = -v with v in [2^-100, 2^126]:
 // s = v*y and h = y/2 from the hardware reciprocal square root y, then the
 // exact remainder d = v - s*s and RN(s + d*h) (checked equal to __fsqrt_rn
-// for every FP32 in [2^-100, 2^128)).
+// for every FP32 in [2^-100, 2^128)). Also v = +0 (nv = -0), for which the
+// result is +0: the approximation reads v + 2^-126, which is v itself for
+// every v >= 2^-100 (2^-126 is below half an ulp there) and a normal number
+// for v = 0, so that y stays finite and s = -0 * y, d and the result are
+// zeros.
 __device__ __forceinline__ f2 neg_sqrt2(f2 nv)
 {
     float v0, v1;
-    unpk(nv, v0, v1);
+    unpk(add2(nv, splat(-0x1p-126f)), v0, v1);
     const f2 y = pk(rsqrt_approx(-v0), rsqrt_approx(-v1));
     const f2 ns = mul2(nv, y);                // -s
     const f2 h = mul2(splat(0.5f), y);

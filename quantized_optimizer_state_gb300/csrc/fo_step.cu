@@ -13,10 +13,12 @@
 // elements (half a group) and loads them with 128-bit streaming loads; the
 // two threads of a group combine their absmax with one shuffle, and the
 // results leave with 128-bit streaming stores. Pairs of elements are computed
-// with packed FP32 instructions and validated fast division and square root;
-// a thread whose operands leave the validated ranges recomputes its 16
-// elements with IEEE operations. Tensor rows travel in the kernel parameters,
-// so a step allocates nothing.
+// with packed FP32 instructions and validated fast division and square root.
+// Exact zeros (zero gradients, momenta and second moments, as in rows that
+// receive no gradient) stay on this path; a thread whose operands leave the
+// validated ranges (a zero theta', a tiny non-zero gradient, extreme
+// hyper-parameters) recomputes its 16 elements with IEEE operations. Tensor
+// rows travel in the kernel parameters, so a step allocates nothing.
 #include <atomic>
 #include <utility>
 
@@ -28,6 +30,17 @@ namespace fo {
 namespace {
 
 constexpr int kEPT = kElemsPerThread;
+
+// AdamW's packed fast path carries the momentum and its companded value z
+// scaled by 2^32 (m' = 2^32 m, z' = 2^32 z): every scaling is exact there and
+// keeps the operands of its divisions inside their validated ranges (see
+// pair_fast). SGD and Lion are unscaled. The exact path delivers z scaled the
+// same way, so the requantization is common.
+template <Opt O> struct ZScale {
+    static constexpr int kInt = O == Opt::kAdamW ? 2 : 1;   // template tag of phi_m_pair
+    static constexpr float up = O == Opt::kAdamW ? 0x1p32f : 1.0f;
+    static constexpr float down = O == Opt::kAdamW ? 0x1p-32f : 1.0f;
+};
 
 
 
@@ -194,7 +207,7 @@ __device__ __forceinline__ void element_exact(const Loaded &L, const uint32_t (&
         nr_out = 0.0f;
     }
     theta_out = theta;
-    z_out = phi_m(m);
+    z_out = __fmul_rn(phi_m(m), ZScale<O>::up);
 }
 
 template <Opt O, int RB, int GB, int... J>
@@ -215,21 +228,43 @@ __device__ __forceinline__ void all_exact(const Loaded &L, const uint32_t (&rx)[
 
 // Running extremes of the fast path's range-checked operands; one check per
 // thread at the end (three-input min/max instead of a compare per element).
+//
+// The checked operand x (the gradient for AdamW, the new momentum for SGD and
+// Lion) may be an exact zero or lie in a range [lo, hi] of magnitudes. A zero
+// is told apart from a tiny value without a compare: c = pattern(x) +
+// 0x7FFFFFFF (mod 2^32) is a NaN for x = +-0 and otherwise a float whose
+// magnitude is the FP32 value just below |x|. min/max ignore NaNs, so the
+// running extremes of |c| see only the non-zero operands.
 struct Guard {
     float min_tp;   // smallest |theta'| (0: a zero theta', exact path)
-    float max_nv;   // largest -v (above -2^-100: v too small for the fast sqrt)
-    float min_q;    // smallest |m/den| first quotient (below 2^-60: exact path)
-    float max_a;    // largest |g| (AdamW, bound 2^24) or |m| (SGD, Lion, bound 2^100)
+    float min_c;    // smallest |c| over non-zero checked operands
+    float max_c;    // largest |c|
     __device__ __forceinline__ void init()
     {
         min_tp = __int_as_float(0x7F800000);
-        max_nv = -__int_as_float(0x7F800000);
-        min_q = __int_as_float(0x7F800000);
-        max_a = 0.0f;
+        min_c = __int_as_float(0x7F800000);
+        max_c = 0.0f;
     }
-    __device__ __forceinline__ bool failed(float max_a_bound) const
+    // both bounds (SGD, Lion: the new momentum)
+    __device__ __forceinline__ void range(float x0, float x1)
     {
-        return !(min_tp > 0.0f) | !(max_nv <= -0x1p-100f) | !(min_q >= 0x1p-60f) | !(max_a <= max_a_bound);
+        const float c0 = __uint_as_float(__float_as_uint(x0) + 0x7FFFFFFFu);
+        const float c1 = __uint_as_float(__float_as_uint(x1) + 0x7FFFFFFFu);
+        min_c = fminf(min_c, fminf(fabsf(c0), fabsf(c1)));
+        max_c = fmaxf(max_c, fmaxf(fabsf(c0), fabsf(c1)));
+    }
+    // the lower bound only (AdamW: the gradient; its upper bound is checked
+    // through sqrt(v), see thread_step)
+    __device__ __forceinline__ void range_lo(float x0, float x1)
+    {
+        const float c0 = __uint_as_float(__float_as_uint(x0) + 0x7FFFFFFFu);
+        const float c1 = __uint_as_float(__float_as_uint(x1) + 0x7FFFFFFFu);
+        min_c = fminf(min_c, fminf(fabsf(c0), fabsf(c1)));
+    }
+    // lo, hi: the bounds on |c| (the FP32 values just below the bounds on |x|)
+    __device__ __forceinline__ bool failed(float lo, float hi) const
+    {
+        return !(min_tp > 0.0f) | !(min_c >= lo) | !(max_c <= hi);
     }
 };
 
@@ -300,17 +335,18 @@ __device__ __forceinline__ f2 mhat_pair(const uint32_t (&mx)[4], const PairConst
 
 // z = phi_m(m) = RN(2m / RN(1 + |m|)), packed, as RN(m / (RN(1 + |m|)/2)):
 // halving is exact and commutes with rounding (the divisor is at least 1/2),
-// so the quotient is the same real number without forming 2m (the fast path
-// keeps |m| far below 2^127, where 2m would overflow). The halved divisor is
-// one fma, RN(-0.5*|m| - 0.5) = -RN(1 + |m|)/2.
+// so the quotient is the same real number without forming 2m. The halved
+// divisor is one fma, RN(-0.5*|m| - 0.5) = -RN(1 + |m|)/2. With ZS = 2^32 the
+// argument is m' = 2^32 m and the result 2^32 z (exact scalings: the fast path
+// keeps them inside the normal range).
+template <int ZS>
 __device__ __forceinline__ f2 phi_m_pair(f2 m)
 {
+    constexpr float kHalfOverZ = ZS == 1 ? -0.5f : -0x1p-33f;
     float m0, m1;
     unpk(m, m0, m1);
-    return div2(m, pk(__fmaf_rn(-0.5f, fabsf(m0), -0.5f), __fmaf_rn(-0.5f, fabsf(m1), -0.5f)));
+    return div2(m, pk(__fmaf_rn(kHalfOverZ, fabsf(m0), -0.5f), __fmaf_rn(kHalfOverZ, fabsf(m1), -0.5f)));
 }
-
-
 
 template <Opt O, int RB, int GB, int W>
 __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[8], const uint32_t (&mx)[4],
@@ -319,13 +355,18 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
 {
     constexpr int j0 = 2 * W, j1 = 2 * W + 1;
     const f2 g = grad_pair<GB, W>(L);
-    float g0, g1;
-    unpk(g, g0, g1);
     const f2 theta = merge_pair<RB, W>(L, rx, gd);
     const f2 mhat = mhat_pair<W>(mx, k);
     f2 thn, m, nrv = 0;
 
     if (O == Opt::kAdamW) {
+        // the gradient decides every operand range: g = 0 or |g| >= lo, with
+        // the host's preconditions and sqrt(v) <= 2^40 (checked in
+        // thread_step), keeps v at 0 or in [2^-100, 2^80] and m at 0 or |m| in
+        // [2^-94, 2^53] (see fo_api.cu)
+        float g0, g1;
+        unpk(g, g0, g1);
+        gd.range_lo(g0, g1);
         // (2^23 + q) as floats -> q * s_v/255 in one fma
         constexpr int b0 = j0 & 3, b1 = j1 & 3;
         const uint32_t vw = L.v[j0 >> 2];
@@ -334,22 +375,11 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
                            k.cv, k.ncv23);
         const f2 vhat = mul2(rq, rq);
         const f2 thd = mul2(theta, k.coef);
-        m = fma2(s.p[0], mhat, mul2(s.p[2], g));                   // b1*m + (1-b1)*g
+        m = fma2(s.p[0], mhat, mul2(s.p[2], g));                   // m' = 2^32 (b1*m + (1-b1)*g)
         const f2 nv = fma2(s.p[1], vhat, mul2(mul2(s.p[3], g), g)); // -(b2*v + ((1-b2)*g)*g)
-        float v0, v1;
-        unpk(nv, v0, v1);
-        // sqrt needs v >= 2^-100; |g| <= 2^24 bounds v (below 2^50), |m|
-        // (below 2^25) and so the divisions' operands from above
-        gd.max_nv = fmaxf(gd.max_nv, fmaxf(v0, v1));
-        gd.max_a = fmaxf(gd.max_a, fmaxf(fabsf(g0), fabsf(g1)));
-        nrv = neg_sqrt2(nv);                                        // -sqrt(v)
+        nrv = neg_sqrt2(nv);                                        // -sqrt(v) (+0 for v = 0)
         const f2 nden = fma2(nrv, s.p[4], s.p[5]);                  // -(sqrt(v)/sqrt(bc2) + eps)
-        f2 q0;
-        const f2 u = div2(m, nden, q0);                             // m / den
-        float q00, q01;
-        unpk(q0, q00, q01);
-        // m/den: a quotient of at least 2^-60 keeps |m| >= 2^-100 (den >= 2^-40)
-        gd.min_q = fminf(gd.min_q, fminf(fabsf(q00), fabsf(q01)));
+        const f2 u = div2(m, nden);                                 // 2^32 m / den
         thn = fma2(s.p[6], u, thd);                                 // theta - lr/bc1 * m/den
     } else if (O == Opt::kSgd) {
         const f2 gp = fma2(k.coef, theta, g);                       // g + wd*theta
@@ -357,7 +387,7 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
         thn = fma2(s.p[1], m, theta);                               // theta - lr*m
         float m0, m1;
         unpk(m, m0, m1);
-        gd.max_a = fmaxf(gd.max_a, fmaxf(fabsf(m0), fabsf(m1)));
+        gd.range(m0, m1);                                           // m = 0 or |m| in [2^-100, 2^100]
     } else {
         const f2 c = fma2(s.p[0], mhat, mul2(s.p[2], g));           // b1*m + (1-b1)*g
         float c0, c1;
@@ -368,10 +398,10 @@ __device__ __forceinline__ void pair_fast(const Loaded &L, const uint32_t (&rx)[
         m = fma2(s.p[1], mhat, mul2(s.p[3], g));                    // b2*m + (1-b2)*g
         float m0, m1;
         unpk(m, m0, m1);
-        gd.max_a = fmaxf(gd.max_a, fmaxf(fabsf(m0), fabsf(m1)));
+        gd.range(m0, m1);                                           // m = 0 or |m| in [2^-100, 2^100]
     }
     unpk(thn, th[j0], th[j1]);
-    unpk(phi_m_pair(m), z[j0], z[j1]);
+    unpk(phi_m_pair<ZScale<O>::kInt>(m), z[j0], z[j1]);
     unpk(nrv, nr[j0], nr[j1]);
 }
 
@@ -415,10 +445,14 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
     const float cv = WithV ? div_by_const(scale_value(L.vs), -255.0f, kRcp255) : 0.0f;
 
     float th[kEPT], z[kEPT], nr[kEPT];
+    float av = 0.0f;   // the thread's largest sqrt(v) (AdamW)
     // the fast path needs the host's range preconditions and a momentum scale
     // below 2 (so that 2 - |z| stays positive); otherwise every element of
     // this thread goes through the exact path
-    bool bad = !s.fast || (L.ms & 0x7FFFu) >= 0x4000u;
+    // (an FP16 pattern of 0x4000 or more is 2.0 or above, infinite, NaN or
+    // negative). AdamW and Lion also need a decay factor of at least 2^-8 in
+    // magnitude, so that a decayed theta is never zero.
+    bool bad = !s.fast || L.ms >= 0x4000u || (O != Opt::kSgd && !(fabsf(row.coef) >= 0x1p-8f));
     if (!bad) {
         PairConsts k;
         k.cm = splat(cm);
@@ -427,12 +461,17 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
         k.coef = splat(row.coef);
         Guard gd;
         gd.init();
-        if (O != Opt::kAdamW) {   // no v and no m/den: those checks pass trivially
-            gd.max_nv = -1.0f;
-            gd.min_q = 1.0f;
-        }
         all_fast<O, RB, GB>(L, rx, mx, s, k, th, z, nr, gd, std::make_integer_sequence<int, kEPT / 2>{});
-        bad = gd.failed(O == Opt::kAdamW ? 0x1p24f : 0x1p100f);
+        bad = gd.failed(s.lo, s.hi);
+        if (WithV) {
+            // the largest sqrt(v), with NaNs propagated: sqrt(v) <= 2^40 bounds
+            // |g| <= 2^52 (v >= (1-b2) g^2 and 1-b2 >= 2^-24), the upper half
+            // of the gradient's range check
+#pragma unroll
+            for (int j = 0; j < kEPT; j += 2)
+                av = max3_nan(av, fabsf(nr[j]), fabsf(nr[j + 1]));
+            bad = bad | !(av <= 0x1p40f);
+        }
     }
     if (bad) {
         // rare: reload (the data is unchanged) and recompute with IEEE operations
@@ -444,6 +483,10 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
         for (int w = 0; w < 4; ++w)
             mx[w] = L.m[w] ^ 0x80808080u;
         all_exact<O, RB, GB>(L, rx, mx, s, row.coef, cm, cv, th, z, nr, std::make_integer_sequence<int, kEPT>{});
+        av = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kEPT; ++j)
+            av = fmaxf(av, fabsf(nr[j]));   // sqrt(v); nr is -sqrt(v)
     }
 
     // re-split theta: theta' (BF16, nearest even) and rho (see split_code;
@@ -476,23 +519,24 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
     // group absmax over this thread's elements, then over the pair. Lanes past
     // the end of the tensor were loaded as zeros and so hold z = 0 and
     // sqrt(v) = 0 exactly: they leave the maxima unchanged.
-    float am = 0.0f, av = 0.0f;
+    // (av, the second moment's, is already formed: on the fast path nr is
+    // -sqrt(v), or +0 for v = 0, and fabs makes both paths agree)
+    float am = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kEPT; ++j) {
+    for (int j = 0; j < kEPT; ++j)
         am = fmaxf(am, fabsf(z[j]));
-        if (WithV)
-            av = fmaxf(av, -nr[j]);
-    }
     am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
     if (WithV)
         av = fmaxf(av, __shfl_xor_sync(0xFFFFFFFFu, av, 1));
 
-    const uint16_t sm_new = scale_of(am);
+    const uint16_t sm_new = scale_of(__fmul_rn(am, ZScale<O>::down));   // exact: am is 2^32 |z| for AdamW
     const uint16_t sv_new = WithV ? scale_of(av) : (uint16_t)0;
     // code multipliers 127/s (m) and 255/s (v), 0 for a zero scale; s is an
     // FP16 value in [2^-24, 65504], inside the validated division range
     const float s_m = scale_value(sm_new), s_v = scale_value(sv_new);
-    const float mult_m = s_m > 0.0f ? div1(127.0f, s_m) : 0.0f;
+    // (for AdamW z holds 2^32 z, so the multiplier is scaled by 2^-32: exact,
+    // and the product z * (127/s) is the same real number)
+    const float mult_m = s_m > 0.0f ? __fmul_rn(div1(127.0f, s_m), ZScale<O>::down) : 0.0f;
     const float mult_v = (WithV && s_v > 0.0f) ? div1(255.0f, s_v) : 0.0f;
     // codes: clamp(rint(x)), x = RN(phi * (L/s)). For m with a normal FP16
     // scale below the 65504 cap the group maximum is at most s*(1 + 2^-11),
@@ -609,10 +653,17 @@ fo_fused_step_kernel(const __grid_constant__ StepParams p)
 template <Opt O, int RB, int GB, bool VNZ, int CH>
 int resident_ctas()
 {
-    // cached after the first successful query; a failed query is not cached,
-    // and its error is consumed so that the launch reports its own status
-    static std::atomic<int> cached{0};
-    int n = cached.load(std::memory_order_relaxed);
+    // per device (up to 64), cached after the first successful query; a
+    // failed query is not cached, and its error is consumed so that the
+    // launch reports its own status
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        (void)cudaGetLastError();
+        dev = 0;
+    }
+    std::atomic<int> &slot = cached[dev & 63];
+    int n = slot.load(std::memory_order_relaxed);
     if (n == 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fo_fused_step_kernel<O, RB, GB, VNZ, CH>, kStepThreads,
                                                           0) != cudaSuccess ||
@@ -620,7 +671,7 @@ int resident_ctas()
             (void)cudaGetLastError();
             return 1;
         }
-        cached.store(n, std::memory_order_relaxed);
+        slot.store(n, std::memory_order_relaxed);
     }
     return n;
 }

@@ -13,6 +13,13 @@ no weights or datasets are used or needed):
 * ``resnet50``   ResNet-50, 161 tensors, 25,557,032 parameters, FlashSGD.
 * ``llama31_8b`` Llama-3.1-8B, 291 tensors, 8,030,261,248 parameters,
                  FlashAdamW (and FlashLion).
+* ``flat_128m``   one flat tensor of 2**27 parameters with the Llama-3.1-8B
+                 table's distributions (weights N(0, 0.02), Student-t(3) x 1e-4
+                 gradients), FlashAdamW: a small case of the same kernel for
+                 DRAM-counter captures.
+* ``gpt2_small_sparse_wte`` the GPT-2 small table whose token-embedding rows
+                 get an exactly zero gradient at every step for a fixed 90 % of
+                 the vocabulary (tokens no batch contains), FlashAdamW.
 * ``stress_64m`` one flat tensor of 2**26 parameters with extreme magnitudes,
                  zeros and BF16 subnormals, FlashAdamW with 8- and 16-bit rho.
 """
@@ -132,6 +139,9 @@ class Workload:
     grad: str                    # "normal", "student_t", "stress"
     grad_scale: float
     rho_bits: int = 8
+    # tensor name -> fraction of its rows (first dimension) whose gradient is
+    # exactly zero at every step (for example embedding rows no token touches)
+    zero_rows: tuple = ()
 
     @property
     def numel(self) -> int:
@@ -157,13 +167,19 @@ def workload(name: str, rho_bits: int = 8) -> Workload:
     if name == "llama31_8b_lion":
         return Workload(name, llama31_8b_params(), "lion", LION_HP, 5, "student_t", 1e-4,
                         rho_bits)
+    if name == "flat_128m":
+        return Workload(name, flat_params(1 << 27), "adamw", ADAMW_HP, 5, "student_t", 1e-4, rho_bits)
+    if name == "gpt2_small_sparse_wte":
+        return Workload(name, gpt2_small_params(), "adamw", ADAMW_HP, 200, "student_t", 1e-4,
+                        rho_bits, zero_rows=(("wte", 0.9),))
     if name == "stress_64m":
         return Workload(name, flat_params(1 << 26, "stress"), "adamw", ADAMW_HP, 20, "stress",
                         1e-3, rho_bits)
     raise KeyError(name)
 
 
-WORKLOADS = ("flat_1m", "gpt2_small", "resnet50", "llama31_8b", "llama31_8b_lion", "stress_64m")
+WORKLOADS = ("flat_1m", "flat_128m", "gpt2_small", "gpt2_small_sparse_wte", "resnet50", "llama31_8b", "llama31_8b_lion",
+             "stress_64m")
 
 # ---------------------------------------------------------------------------
 # Seeded generators (host, numpy)
@@ -304,3 +320,44 @@ def grad_fp32_device(kind: str, scale: float, n: int, tensor_index: int, step: i
     else:
         raise KeyError(kind)
     return x
+
+
+# ---------------------------------------------------------------------------
+# Gradients of a workload's tensor (with its all-zero rows)
+# ---------------------------------------------------------------------------
+
+ZERO_ROW_SEED = 7
+
+
+def zero_row_mask(w: Workload, tensor_index: int):
+    """Boolean mask over the first dimension of tensor ``tensor_index``: the rows
+    whose gradient is zero at every step, or None."""
+    spec = w.params[tensor_index]
+    frac = dict(w.zero_rows).get(spec.name)
+    if not frac:
+        return None
+    return _rng(ZERO_ROW_SEED, tensor_index).random(spec.shape[0]) < frac
+
+
+def workload_grad_fp32(w: Workload, tensor_index: int, step: int) -> np.ndarray:
+    spec = w.params[tensor_index]
+    g = grad_fp32(w.grad, w.grad_scale, spec.numel, tensor_index, step)
+    mask = zero_row_mask(w, tensor_index)
+    if mask is not None:
+        g.reshape(spec.shape[0], -1)[mask] = 0.0
+    return g
+
+
+def workload_grad_bf16(w: Workload, tensor_index: int, step: int) -> np.ndarray:
+    return to_bf16_bits(workload_grad_fp32(w, tensor_index, step))
+
+
+def workload_grad_device(w: Workload, tensor_index: int, step: int, device, fp32: bool = False):
+    """The tensor's gradient drawn on the device (BF16, or FP32 with fp32=True)."""
+    import torch
+    spec = w.params[tensor_index]
+    g = grad_fp32_device(w.grad, w.grad_scale, spec.numel, tensor_index, step, device)
+    mask = zero_row_mask(w, tensor_index)
+    if mask is not None:
+        g.view(spec.shape[0], -1)[torch.from_numpy(mask).to(g.device)] = 0.0
+    return g if fp32 else g.to(torch.bfloat16)

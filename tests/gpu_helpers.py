@@ -106,3 +106,41 @@ def assert_state_matches(d: "oracle.State", ref: "oracle.State", what: str, n_to
     if ref.v_q is not None:
         assert_codes(d.v_q, ref.v_q, what + " v codes", n_total)
         assert_scales(d.v_scale, ref.v_scale, what + " v scales")
+
+
+def _chunks_of(st: "oracle.State", g: np.ndarray, chunk: int):
+    """Group-aligned pieces of one state (views: the oracle updates them in place)."""
+    n = st.numel
+    out = []
+    for lo in range(0, n, chunk):
+        hi = min(n, lo + chunk)
+        g0, g1 = lo // 32, (hi + 31) // 32
+        sub = oracle.State(st.theta_p[lo:hi], st.rho[lo:hi], st.m_q[lo:hi], st.m_scale[g0:g1],
+                           None if st.v_q is None else st.v_q[lo:hi],
+                           None if st.v_scale is None else st.v_scale[g0:g1],
+                           st.weight_decay, st.rho_bits)
+        out.append((sub, np.ascontiguousarray(g[lo:hi])))
+    return out
+
+
+_POOL = None
+
+
+def oracle_step_parallel(opt: str, states, grads, t: int, hp: dict, chunk: int = 1 << 20):
+    """One oracle step over large states, cut into group-aligned chunks that
+    run on a thread per host core (groups are independent, so this equals one
+    call over the whole table; the oracle itself is unchanged)."""
+    import concurrent.futures as cf
+    import os
+    global _POOL
+    if _POOL is None:
+        _POOL = cf.ThreadPoolExecutor(max(1, len(os.sched_getaffinity(0))))
+    pieces = [p for st, g in zip(states, grads) for p in _chunks_of(st, g, chunk)]
+    if opt == "adamw":
+        f = lambda p: oracle.adamw_step([p[0]], [p[1]], hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], t,
+                                        v_nonzero=hp.get("v_nonzero", False))
+    elif opt == "sgd":
+        f = lambda p: oracle.sgd_step([p[0]], [p[1]], hp["lr"], hp["momentum"])
+    else:
+        f = lambda p: oracle.lion_step([p[0]], [p[1]], hp["lr"], hp["beta1"], hp["beta2"])
+    list(_POOL.map(f, pieces))

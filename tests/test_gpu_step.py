@@ -255,14 +255,19 @@ def _device_workload(w, grad_fp32=False):
 
 @pytest.mark.parametrize("name", ["llama31_8b", "llama31_8b_lion"])
 def test_llama31_8b_full_size_sampled(name):
-    """The full 8.03e9-parameter table in one call (the benchmarked launch), with
-    every row sampled at its head, middle and tail and checked against the oracle."""
+    """The full 8.03e9-parameter table in one call (the benchmarked launch), for
+    all five steps of the run, with every eighth row (and the first and last
+    ones) sampled at its head, middle and tail and checked against the oracle."""
     w = wl.workload(name)
     dev, grads = _device_workload(w)
     hp, _ = _hp(w)
     rows = set(range(0, len(w.params), 8)) | {0, 1, 2, 3, 4, 5, 6, 7, len(w.params) - 2, len(w.params) - 1}
     samples = _samples_of([p.numel for p in w.params], rows=rows)
-    for t in (1, 2):
+    for t in range(1, w.steps + 1):                # all 5 steps, a fresh gradient each
+        if t > 1:
+            for i in range(len(grads)):
+                grads[i] = None
+                grads[i] = wl.workload_grad_device(w, i, t, "cuda")
         _sampled_parity(w.optimizer, dev, grads, samples, t, hp)
     del dev, grads
     torch.cuda.empty_cache()
@@ -280,3 +285,29 @@ def test_tensor_larger_than_2_to_31_elements():
     _sampled_parity("adamw", [d], [g], samples, 1, ADAMW)
     del d, g
     torch.cuda.empty_cache()
+
+
+def test_rows_may_share_a_gradient():
+    """Gradients are only read: two rows stepped from one gradient tensor are
+    accepted and each matches the oracle."""
+    rng = np.random.default_rng(31)
+    thetas = [(rng.standard_normal(5000) * 0.02).astype(np.float32) for _ in range(2)]
+    dev = _make_states(thetas, "adamw", 8, 0.01)
+    for t in (1, 2, 3):
+        g = wl.to_bf16_bits((rng.standard_normal(5000) * 1e-3).astype(np.float32))
+        gd = to_dev(g)
+        ref = [oracle_state_from_device(d) for d in dev]
+        _oracle_step("adamw", ref, [g, g], t, ADAMW)
+        _gpu_step("adamw", dev, [gd, gd], t, ADAMW)          # one device tensor in both rows
+        for i, d in enumerate(dev):
+            assert_state_matches(oracle_state_from_device(d), ref[i], f"shared gradient step {t} row {i}")
+
+
+def test_device_check_on_a_real_tensor(monkeypatch):
+    d = fo.CompressedTensor(64, "cuda:0", 8, True, 0.0)
+    g = torch.zeros(64, dtype=torch.bfloat16, device="cuda:0")
+    with torch.cuda.device(0):
+        assert fo.row(d.theta, d.rho, d.m_q, d.m_scale, g, d.v_q, d.v_scale).numel == 64
+    monkeypatch.setattr(fo, "_current_device", lambda: 1)
+    with pytest.raises(ValueError, match="current device"):
+        fo.row(d.theta, d.rho, d.m_q, d.m_scale, g, d.v_q, d.v_scale)
