@@ -59,6 +59,14 @@ def parse_args(argv=None):
                    help="time budget of the CPU oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--record-traffic", metavar="CSV:WORKLOAD[,CSV:WORKLOAD]",
+                   help="store the DRAM bytes per parameter of ncu --csv captures of one step-kernel launch each "
+                        "(two sizes: the slope between them) for --rho-bits, --grad-dtype, and exit")
+    p.add_argument("--traffic-command", default=None, help="the ncu command line, recorded with --record-traffic")
+    p.add_argument("--grad-release", action="store_true",
+                   help="time gradient release against a plain step() on --workload (GPT-2 small by default) and exit")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="skip timing the other workloads (flat 1M, GPT-2 small, ResNet-50, Lion 8B, stress set)")
     return p.parse_args(argv)
 
 
@@ -139,7 +147,7 @@ class OracleSample:
             p = w.params[i]
             st = oracle.State.from_fp32(wl.init_weight(p, i), rho_bits, with_v,
                                         w.hparams["weight_decay"])
-            g = (wl.grad_fp32 if grad_dtype == "f32" else wl.grad_bf16)(w.grad, w.grad_scale, p.numel, i, 1)
+            g = (wl.workload_grad_fp32 if grad_dtype == "f32" else wl.workload_grad_bf16)(w, i, 1)
             self.states.append(st)
             self.grads.append(g)
             for lo in range(0, p.numel, chunk):
@@ -285,9 +293,10 @@ def _gpu_id_for_smi(device_index: int) -> str:
 # The GPU arm
 # ---------------------------------------------------------------------------
 
-PROFILE = os.path.join(ROOT, "profiles", "fo_fused_step_kernel_adamw_llama31_8b.md")
-
-
+# DRAM traffic of the step kernel, captured with ncu on a small case and
+# stored per parameter (see record_traffic); valid while the sources hash to
+# the captured version.
+TRAFFIC = os.path.join(ROOT, "profiles", "fo_fused_step_kernel_traffic.json")
 STEP_SOURCES = ("fo_api.cu", "fo_device.cuh", "fo_internal.h", "fo_pair.cuh", "fo_step.cu")
 
 
@@ -307,23 +316,85 @@ def _kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def _profiled_traffic(workload: str, rho_bits: int, grad_dtype: str = "bf16"):
-    """DRAM bytes per launch from the committed ncu capture of the default
-    workload, or None when the kernel sources changed since that capture."""
-    if workload != "llama31_8b" or rho_bits != 8 or grad_dtype != "bf16":
-        return None
+def _traffic_key(optimizer: str, rho_bits: int, grad_dtype: str) -> str:
+    return f"{optimizer}_rho{rho_bits}_{grad_dtype}"
+
+
+def _profiled_traffic(optimizer: str, rho_bits: int, grad_dtype: str, params: int):
+    """DRAM bytes per launch for a table of `params` parameters: the captured
+    bytes per parameter of this kernel variant times the parameters, or None
+    when no capture matches the current sources."""
     try:
-        text = open(PROFILE).read()
-    except OSError:
+        with open(TRAFFIC) as f:
+            rec = json.load(f).get(_traffic_key(optimizer, rho_bits, grad_dtype))
+    except (OSError, ValueError):
         return None
-    fields = dict(line.split(":", 1) for line in text.splitlines()
-                  if line.startswith(("source_sha256_16:", "traffic_bytes_per_launch:")))
-    if fields.get("source_sha256_16", "").strip() != _kernel_source_hash():
+    if not rec or rec.get("source_sha256_16") != _kernel_source_hash():
         return None
+    return float(rec["dram_bytes_per_param"]) * params
+
+
+def _ncu_bytes(csv_path: str) -> float:
+    """dram__bytes_read.sum + dram__bytes_write.sum of the one fused-step launch
+    in an ncu --csv log."""
+    import csv
+    scale = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12}
+    with open(csv_path) as f:
+        lines = f.read().splitlines()
+    start = next(i for i, l in enumerate(lines) if l.startswith('"ID"'))
+    rows = list(csv.reader(lines[start:]))
+    h = rows[0]
+    k, m, u, v = (h.index(x) for x in ("Kernel Name", "Metric Name", "Metric Unit", "Metric Value"))
+    got = {}
+    for r in rows[1:]:
+        if len(r) > v and "fo_fused_step_kernel" in r[k] and r[m] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            got.setdefault(r[m], []).append(float(r[v].replace(",", "")) * scale[r[u]])
+    if set(got) != {"dram__bytes_read.sum", "dram__bytes_write.sum"} or len(got["dram__bytes_read.sum"]) != 1:
+        raise SystemExit(f"{csv_path}: expected one fused-step launch with both DRAM byte counters")
+    return got["dram__bytes_read.sum"][0] + got["dram__bytes_write.sum"][0]
+
+
+def record_traffic(args):
+    """Store the DRAM bytes per parameter of the step kernel in TRAFFIC, keyed by
+    kernel variant and stamped with the current source hash. args.record_traffic
+    lists ncu --csv captures (one launch each, counters dram__bytes_read.sum and
+    dram__bytes_write.sum) as CSV:WORKLOAD items separated by commas. With two
+    captures of different sizes the figure is the slope between them: at the end
+    of a launch up to an L2's worth of written lines can still sit in L2 (written
+    back later), a constant that the difference cancels. With one capture it is
+    that capture's bytes over its parameters."""
+    from quantized_optimizer_state_gb300 import workloads as wl
+    caps = []
+    for item in args.record_traffic.split(","):
+        path, _, name = item.partition(":")
+        w = wl.workload(name or args.workload, args.rho_bits)
+        caps.append((w, _ncu_bytes(path)))
+    caps.sort(key=lambda c: c[0].numel)
+    w = caps[-1][0]
+    if len(caps) >= 2:
+        (w0, b0), (w1, b1) = caps[0], caps[-1]
+        per_param = (b1 - b0) / (w1.numel - w0.numel)
+        how = f"slope between {w0.name} ({b0:.0f} B) and {w1.name} ({b1:.0f} B)"
+    else:
+        per_param = caps[0][1] / w.numel
+        how = f"{w.name}: {caps[0][1]:.0f} B over its parameters"
     try:
-        return float(fields["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+        with open(TRAFFIC) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        data = {}
+    key = _traffic_key(w.optimizer, args.rho_bits, args.grad_dtype)
+    data[key] = {
+        "source_sha256_16": _kernel_source_hash(), "captures": [[c[0].name, c[0].numel, c[1]] for c in caps],
+        "dram_bytes_per_param": per_param, "derivation": how,
+        "algorithmic_bytes_per_param": _algo_bytes(w, args.rho_bits, args.grad_dtype),
+        "command": args.traffic_command or "",
+    }
+    with open(TRAFFIC, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps(data[key]))
+    return 0
 
 
 def _measured_peak():
@@ -357,7 +428,6 @@ def _build_states(w, rho_bits, device, grad_dtype="bf16"):
     flat_theta = torch.empty(total, dtype=torch.int16, device=device)
     flat_grad = torch.empty(total, dtype=gdt, device=device)
     states, grads = [], []
-    gen = wl.grad_fp32_device if grad_dtype == "f32" else wl.grad_bf16_device
     for i, p in enumerate(w.params):
         o = offs[i]
         d = fo.CompressedTensor(p.numel, device, rho_bits, w.optimizer == "adamw",
@@ -367,7 +437,7 @@ def _build_states(w, rho_bits, device, grad_dtype="bf16"):
         del theta
         states.append(d)
         g = flat_grad[o:o + p.numel]
-        g.copy_(gen(w.grad, w.grad_scale, p.numel, i, 1, device))
+        g.copy_(wl.workload_grad_device(w, i, 1, device, fp32=grad_dtype == "f32"))
         grads.append(g)
     torch.cuda.synchronize(device)
     return states, grads, {"theta": flat_theta, "grad": flat_grad, "offs": offs}
@@ -485,6 +555,14 @@ def run_ours(args):
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.rho_bits, args.cpu_seconds, args.grad_dtype)
 
+    # the other configurations, one at a time after the headline's state is freed
+    per_config = None
+    if ws == 1 and not args.no_per_config:
+        del table, step, states, grads, flat
+        torch.cuda.empty_cache()
+        per_config = {key: measure_config(name, rb, steps, 5, flush, device, stream)
+                      for key, name, rb, steps, flush in PER_CONFIG}
+
     if rank == 0:
         peak, peak_kind = _measured_peak()
         algo = _algo_bytes(w, args.rho_bits, args.grad_dtype) * w.numel
@@ -496,7 +574,8 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": _config(w, args.rho_bits, ws, args.grad_dtype),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": _profiled_traffic(args.workload, args.rho_bits, args.grad_dtype),
+                         "frac": achieved / peak,
+                         "traffic": _profiled_traffic(w.optimizer, args.rho_bits, args.grad_dtype, w.numel),
                          "kernel": f"fo_fused_step_kernel<{w.optimizer}>",
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback 6.8 TB/s",
@@ -506,11 +585,74 @@ def run_ours(args):
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "per_config": per_config,
         }
         print(json.dumps(out), flush=True)
     if ws > 1:
         dist.destroy_process_group()
     return 0
+
+
+# ---------------------------------------------------------------------------
+# Per-configuration figures (each of the other workloads, timed the same way)
+# ---------------------------------------------------------------------------
+
+# (key, workload, rho_bits, timed steps, flush L2 between steps). The 2^20-
+# parameter step moves 12.8 MB, which fits in L2: it is timed as latency with
+# a 512 MB write between steps, so every step starts from DRAM. The others
+# stream far more than L2 holds per step.
+PER_CONFIG = (
+    ("flat_1m", "flat_1m", 8, 200, True),
+    ("gpt2_small", "gpt2_small", 8, 300, False),
+    ("gpt2_small_sparse_wte", "gpt2_small_sparse_wte", 8, 300, False),
+    ("resnet50", "resnet50", 8, 500, False),
+    ("llama31_8b_lion", "llama31_8b_lion", 8, 40, False),
+    ("stress_64m_rho8", "stress_64m", 8, 100, False),
+    ("stress_64m_rho16", "stress_64m", 16, 100, False),
+)
+L2_FLUSH_BYTES = 512 << 20
+
+
+def measure_config(name, rho_bits, steps, warmup, flush, device, stream):
+    """Time `steps` fused steps of workload `name` (one seeded gradient set),
+    each bracketed by CUDA events on the launching stream; returns the
+    per-configuration record."""
+    import torch
+    from quantized_optimizer_state_gb300 import fo
+    from quantized_optimizer_state_gb300 import workloads as wl
+    w = wl.workload(name, rho_bits)
+    states, grads, flat = _build_states(w, rho_bits, device)
+    step = _stepper(w, fo.table_of(states, grads))
+    scratch = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device) if flush else None
+    t = 0
+    for _ in range(warmup):
+        t += 1
+        step(t, stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize(device)
+    w0 = time.perf_counter()
+    for k in range(steps):
+        t += 1
+        if scratch is not None:
+            scratch.fill_(k & 0xFF)
+        ev[k][0].record(stream)
+        step(t, stream)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - w0
+    ms = [a.elapsed_time(b) for a, b in ev]
+    del states, grads, flat, scratch
+    torch.cuda.empty_cache()
+    peak, _ = _measured_peak()
+    algo = _algo_bytes(w, rho_bits) * w.numel
+    mean = statistics.mean(ms)
+    return {"workload": name, "optimizer": w.optimizer, "rho_bits": rho_bits, "params": w.numel,
+            "tensors": len(w.params), "steps": steps, "kernel_ms": mean, "kernel_ms_median": statistics.median(ms),
+            "kernel_ms_min": min(ms), "ms_per_step": None if flush else 1e3 * wall / steps,
+            "params_per_s": w.numel / (mean * 1e-3), "gbs": algo / (mean * 1e-3) / 1e9,
+            "frac": algo / (mean * 1e-3) / 1e9 / peak, "algorithmic_bytes_per_step": algo,
+            "timing": ("latency: CUDA events around each step, 512 MB written between steps (L2 flushed)"
+                       if flush else "CUDA events around each step; each step streams more than L2 holds")}
 
 
 def _chunks(sizes, n_chunks):
@@ -526,6 +668,57 @@ def _chunks(sizes, n_chunks):
     if cur:
         out.append(cur)
     return out
+
+
+def _async_engine_count(device_index: int):
+    """cudaDevAttrAsyncEngineCount of the device (copy engines that can run
+    concurrently with kernels and each other), read through the CUDA runtime;
+    None if the runtime library cannot be found."""
+    import ctypes
+    import glob
+    cands = ["libcudart.so", "libcudart.so.13", "libcudart.so.12"]
+    cands += sorted(glob.glob("/usr/local/cuda/lib64/libcudart.so*"))
+    for name in cands:
+        try:
+            rt = ctypes.CDLL(name)
+        except OSError:
+            continue
+        v = ctypes.c_int(0)
+        if rt.cudaDeviceGetAttribute(ctypes.byref(v), 40, device_index) == 0:   # cudaDevAttrAsyncEngineCount
+            return int(v.value)
+    return None
+
+
+def _link_rates(h_src, d_dst, d_src, h_dst, nbytes, stream_a, stream_b, device):
+    """Host-link rates (GB/s) with pinned buffers: host -> device alone, device
+    -> host alone, and both at once on two streams (best of three each)."""
+    import torch
+    n_in = nbytes // h_src.element_size()
+    n_out = nbytes // h_dst.element_size()
+
+    def timed(fn):
+        best = float("inf")
+        for _ in range(3):
+            torch.cuda.synchronize(device)
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(device)
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(stream_a):
+            d_dst[:n_in].copy_(h_src[:n_in], non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(stream_b):
+            h_dst[:n_out].copy_(d_src[:n_out], non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+    return {"h2d_gbs": nbytes / timed(h2d) / 1e9, "d2h_gbs": nbytes / timed(d2h) / 1e9,
+            "both_directions_gbs": 2 * nbytes / timed(both) / 1e9, "probe_bytes": nbytes}
 
 
 def _e2e(w, states, grads, flat, step_fn_of, stream, device, steps, t, barrier, reduce, ws, n_chunks=16,
@@ -551,6 +744,10 @@ def _e2e(w, states, grads, flat, step_fn_of, stream, device, steps, t, barrier, 
     ranges = [(offs[c[0]], offs[c[-1]] + sizes[c[-1]]) for c in chunks]
     steppers = [step_fn_of(fo.table_of([states[i] for i in c], [grads[i] for i in c])) for c in chunks]
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    # what the host link and the copy engines allow on this machine, measured
+    # before the timed region (the end-to-end time is bound by them)
+    link = _link_rates(h_grad, f_grad, f_theta, h_out, min(1 << 30, h_out.numel() * 2), s_in, s_out, device)
+    link["copy_engines"] = _async_engine_count(device.index if device.index is not None else 0)
     ev_in = [torch.cuda.Event() for _ in chunks]
     ev_done = [torch.cuda.Event() for _ in chunks]
     g_piece = max(1, piece_bytes // f_grad.element_size())
@@ -592,14 +789,93 @@ def _e2e(w, states, grads, flat, step_fn_of, stream, device, steps, t, barrier, 
     barrier()
     ms = reduce(e0.elapsed_time(e1), "max")
     return {"value": job_throughput(ws, w.numel, steps, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps, "link": link,
             "path": f"pinned host {str(f_grad.dtype).split('.')[-1]} grads -> device, fused step,"
                     f" theta' -> pinned host; {len(chunks)} tensor chunks pipelined on copy-in/compute/"
                     f"copy-out streams, copies in {piece_bytes >> 20} MB pieces of flat buffers"}
 
 
+# ---------------------------------------------------------------------------
+# Gradient release against a plain optimizer step (drop-in optimizers)
+# ---------------------------------------------------------------------------
+
+def grad_release_study(name="gpt2_small", iters=20, warmup=5):
+    """Backward + FlashAdamW step of a table's parameters three ways: a plain
+    step() after backward, gradient release in buckets (the default size) and
+    release of every parameter on its own. The backward pass is synthetic (the
+    loss is sum(p * c) for a fixed random c per parameter, so each gradient is
+    c in BF16), identical in all three. Reported per iteration: the whole
+    iteration (host wall time), the host time spent in the optimizer's
+    stepping code, the GPU time of the optimizer's work (CUDA events around
+    each of its calls) and its kernel launches."""
+    import torch
+    from quantized_optimizer_state_gb300 import fo, optim
+    from quantized_optimizer_state_gb300 import workloads as wl
+    w = wl.workload(name)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    def make():
+        ps, cs = [], []
+        for i, p in enumerate(w.params):
+            x = wl.init_weight_device(p, i, dev).view(p.shape)
+            ps.append(torch.nn.Parameter(x))
+            cs.append(wl.workload_grad_device(w, i, 1, dev).view(p.shape))
+        opt = optim.FlashAdamW(ps, lr=w.hparams["lr"], betas=(w.hparams["beta1"], w.hparams["beta2"]),
+                               eps=w.hparams["eps"], weight_decay=w.hparams["weight_decay"])
+        return ps, cs, opt
+
+    out = {"study": "grad_release", "workload": name, "params": w.numel, "tensors": len(w.params),
+           "iters": iters}
+    for mode, bucket in (("plain_step", None), ("release_bucketed", 1 << 24), ("release_per_parameter", 0)):
+        ps, cs, opt = make()
+        calls = []                      # (host seconds, start event, end event) per optimizer call
+        inner = opt._step_params
+
+        def timed_step_params(params, group, inner=inner, calls=calls):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0 = time.perf_counter()
+            e0.record()
+            inner(params, group)
+            e1.record()
+            calls.append((time.perf_counter() - t0, e0, e1))
+        opt._step_params = timed_step_params
+        if bucket is not None:
+            opt.attach_grad_release(bucket_numel=bucket)
+
+        def one():
+            sum((p * c).float().sum() for p, c in zip(ps, cs)).backward()
+            if bucket is None:
+                opt.step()
+                opt.zero_grad(set_to_none=True)
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize(dev)
+        calls.clear()
+        l0 = fo.fo_kernel_launch_count()
+        t0 = time.perf_counter()
+        for _ in range(iters):
+            one()
+        torch.cuda.synchronize(dev)
+        total = (time.perf_counter() - t0) * 1e3 / iters
+        out[mode] = {"iteration_ms": total,
+                     "optimizer_host_ms": 1e3 * sum(c[0] for c in calls) / iters,
+                     "optimizer_gpu_ms": sum(c[1].elapsed_time(c[2]) for c in calls) / iters,
+                     "optimizer_calls": len(calls) / iters,
+                     "optimizer_launches": (fo.fo_kernel_launch_count() - l0) / iters,
+                     "bucket_numel": bucket}
+        del ps, cs, opt, calls
+        torch.cuda.empty_cache()
+    return out
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.record_traffic:
+        return record_traffic(args)
+    if args.grad_release:
+        print(json.dumps(grad_release_study(args.workload if args.workload != "llama31_8b" else "gpt2_small")),
+              flush=True)
+        return 0
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -13,7 +13,7 @@ no weights or datasets are used or needed):
 * ``resnet50``   ResNet-50, 161 tensors, 25,557,032 parameters, FlashSGD.
 * ``llama31_8b`` Llama-3.1-8B, 291 tensors, 8,030,261,248 parameters,
                  FlashAdamW (and FlashLion).
-* ``flat_128m``   one flat tensor of 2**27 parameters with the Llama-3.1-8B
+* ``flat_128m``, ``flat_256m`` one flat tensor of 2**27 or 2**28 parameters with the Llama-3.1-8B
                  table's distributions (weights N(0, 0.02), Student-t(3) x 1e-4
                  gradients), FlashAdamW: a small case of the same kernel for
                  DRAM-counter captures.
@@ -169,6 +169,8 @@ def workload(name: str, rho_bits: int = 8) -> Workload:
                         rho_bits)
     if name == "flat_128m":
         return Workload(name, flat_params(1 << 27), "adamw", ADAMW_HP, 5, "student_t", 1e-4, rho_bits)
+    if name == "flat_256m":
+        return Workload(name, flat_params(1 << 28), "adamw", ADAMW_HP, 5, "student_t", 1e-4, rho_bits)
     if name == "gpt2_small_sparse_wte":
         return Workload(name, gpt2_small_params(), "adamw", ADAMW_HP, 200, "student_t", 1e-4,
                         rho_bits, zero_rows=(("wte", 0.9),))
@@ -178,7 +180,7 @@ def workload(name: str, rho_bits: int = 8) -> Workload:
     raise KeyError(name)
 
 
-WORKLOADS = ("flat_1m", "flat_128m", "gpt2_small", "gpt2_small_sparse_wte", "resnet50", "llama31_8b", "llama31_8b_lion",
+WORKLOADS = ("flat_1m", "flat_128m", "flat_256m", "gpt2_small", "gpt2_small_sparse_wte", "resnet50", "llama31_8b", "llama31_8b_lion",
              "stress_64m")
 
 # ---------------------------------------------------------------------------

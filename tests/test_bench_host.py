@@ -103,3 +103,43 @@ def test_flat_offsets_are_aligned_and_disjoint():
     ends = [o + n for o, n in zip(offs, sizes)]
     assert all(e <= o2 for e, o2 in zip(ends, offs[1:])) and ends[-1] <= total
     assert total - sum(sizes) < 64 * len(sizes)
+
+
+_NCU_CSV = '''==PROF== Connected to process 1
+"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream","Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit","Metric Value"
+"0","1","python","h","void fo::split_kernel<8>(const float *, unsigned short *, void *, long)","1","7","(256, 1, 1)","(456, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_read.sum","Mbyte","999.00"
+"1","1","python","h","void fo::<unnamed>::fo_fused_step_kernel<(fo::Opt)0, 8, 16, false, 8>(fo::StepParams)","1","7","(256, 1, 1)","(456, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_read.sum","Gbyte","1.10"
+"1","1","python","h","void fo::<unnamed>::fo_fused_step_kernel<(fo::Opt)0, 8, 16, false, 8>(fo::StepParams)","1","7","(256, 1, 1)","(456, 1, 1)","0","10.3","Command line profiler metrics","dram__bytes_write.sum","Mbyte","550.50"
+'''
+
+
+def test_traffic_record_is_per_parameter_and_keyed_to_the_sources(tmp_path, monkeypatch):
+    """An ncu capture of one step-kernel launch on a small case becomes DRAM
+    bytes per parameter; bench scales it to a table and drops it once the
+    kernel sources change."""
+    csv_path = tmp_path / "traffic.csv"
+    csv_path.write_text(_NCU_CSV)
+    monkeypatch.setattr(bench, "TRAFFIC", str(tmp_path / "traffic.json"))
+    assert bench._ncu_bytes(str(csv_path)) == 1.10e9 + 550.5e6
+    assert bench.main(["--record-traffic", f"{csv_path}:flat_256m", "--traffic-command", "ncu ..."]) == 0
+    rec = json.load(open(tmp_path / "traffic.json"))["adamw_rho8_bf16"]
+    assert rec["dram_bytes_per_param"] == (1.10e9 + 550.5e6) / (1 << 28)
+    # two sizes: the slope, which cancels a constant (lines still in L2 at the end)
+    small = tmp_path / "small.csv"
+    small.write_text(_NCU_CSV.replace('"1.10"', '"0.50"'))
+    assert bench.main(["--record-traffic", f"{csv_path}:flat_256m,{small}:flat_128m"]) == 0
+    rec = json.load(open(tmp_path / "traffic.json"))["adamw_rho8_bf16"]
+    assert rec["dram_bytes_per_param"] == (1.10e9 - 0.50e9) / ((1 << 28) - (1 << 27))
+    assert bench._profiled_traffic("adamw", 8, "bf16", 1000) == rec["dram_bytes_per_param"] * 1000
+    assert bench._profiled_traffic("lion", 8, "bf16", 1000) is None
+    monkeypatch.setattr(bench, "_kernel_source_hash", lambda: "0" * 16)
+    assert bench._profiled_traffic("adamw", 8, "bf16", 1000) is None
+
+
+def test_per_config_covers_the_other_configurations():
+    keys = {k for k, *_ in bench.PER_CONFIG}
+    assert {"flat_1m", "gpt2_small", "resnet50", "llama31_8b_lion", "stress_64m_rho8",
+            "stress_64m_rho16", "gpt2_small_sparse_wte"} <= keys
+    flush = {k: f for k, _, _, _, f in bench.PER_CONFIG}
+    assert flush["flat_1m"] and not flush["gpt2_small"]        # only the L2-sized step is flushed
+    assert bench.L2_FLUSH_BYTES > 129e6
