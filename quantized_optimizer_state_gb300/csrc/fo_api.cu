@@ -202,9 +202,11 @@ fo_status_t run_table(Opt opt, const fo_tensor_t *table, int32_t ntensors, const
                 total += table[j].numel;
         if (total == 0)
             continue;
-        const int64_t want_tiles = (int64_t)fo::sm_count() * fo::step_ctas_per_sm(opt) * fo::kMinTilesPerCta;
-        const int chunks = total / ((int64_t)fo::kStepChunk * fo::kLongChunks) >= want_tiles ? fo::kLongChunks
-                                                                                            : fo::kShortChunks;
+        const int64_t ctas = (int64_t)fo::sm_count() * fo::step_ctas_per_sm(opt);
+        const int chunks = total / ((int64_t)fo::kStepChunk * fo::kLongChunks) >= ctas * fo::kMinTilesPerCta
+                               ? fo::kLongChunks
+                           : total / ((int64_t)fo::kStepChunk * fo::kShortChunks) >= ctas ? fo::kShortChunks
+                                                                                           : fo::kTinyChunks;
         p.chunks = chunks;
         const int64_t tile_elems = (int64_t)fo::kStepChunk * chunks;
         int32_t i = 0;

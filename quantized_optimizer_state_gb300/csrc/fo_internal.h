@@ -16,11 +16,14 @@ constexpr int kStepThreads = FO_STEP_THREADS;
 constexpr int kStepChunk = kStepThreads * kElemsPerThread;  // 4096 elements
 // A tile is `chunks` consecutive chunks of one row, stepped by one CTA one
 // after the other (they share the row lookup and per-row constants). The
-// kernel is compiled for kLongChunks and kShortChunks chunks per tile; the
-// host takes the long tiles when they still give every resident CTA at least
-// kMinTilesPerCta tiles (large tables), the short ones otherwise.
+// kernel is compiled for kLongChunks, kShortChunks and kTinyChunks chunks per
+// tile; the host takes the long tiles when they still give every resident CTA
+// at least kMinTilesPerCta tiles (large tables), the short ones otherwise,
+// and one-chunk tiles when short ones would leave CTAs without a tile (tables
+// of a few million elements, whose step is latency: more CTAs at work).
 constexpr int kLongChunks = 8;
 constexpr int kShortChunks = 2;
+constexpr int kTinyChunks = 1;
 constexpr int kMinTilesPerCta = 8;
 
 
@@ -80,7 +83,7 @@ struct StepParams {
     StepScalars s;
     int32_t nrows;
     int32_t total_tiles;
-    int32_t chunks;                    // chunks per tile: kLongChunks or kShortChunks
+    int32_t chunks;                    // chunks per tile: kLongChunks, kShortChunks or kTinyChunks
     int32_t pad;
     int32_t tile_end[kRowsPerLaunch];  // inclusive prefix sums of tiles per row
     StepRow rows[kRowsPerLaunch];

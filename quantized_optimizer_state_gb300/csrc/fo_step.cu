@@ -689,8 +689,11 @@ cudaError_t launch_ch(const StepParams &p, cudaStream_t stream)
 template <Opt O, int RB, int GB, bool VNZ = false>
 cudaError_t launch(const StepParams &p, cudaStream_t stream)
 {
-    return p.chunks == kLongChunks ? launch_ch<O, RB, GB, VNZ, kLongChunks>(p, stream)
-                                   : launch_ch<O, RB, GB, VNZ, kShortChunks>(p, stream);
+    if (p.chunks == kLongChunks)
+        return launch_ch<O, RB, GB, VNZ, kLongChunks>(p, stream);
+    if (p.chunks == kShortChunks)
+        return launch_ch<O, RB, GB, VNZ, kShortChunks>(p, stream);
+    return launch_ch<O, RB, GB, VNZ, kTinyChunks>(p, stream);
 }
 
 template <int RB, int GB>

@@ -1,11 +1,14 @@
-"""Parity of every step kernel, for both tile lengths the library launches.
+"""Parity of every step kernel, for the three tile lengths the library launches.
 
 Long tiles (8 chunks of 4096 elements) are used for tables large enough to
 give each resident CTA at least 8 of them (about 120M elements). Each long
 case is one row of 2^27 elements, checked against the oracle on chunks at its
 head, middle and tail over two steps (groups are independent, so a chunk's
 oracle step needs only that chunk's state). Short tiles (2 chunks) serve
-smaller tables. Each short case is a small ragged table, checked in full."""
+tables that still give every CTA a tile (a few million elements up); each
+short case is a ragged table of about 6M elements, sampled the same way.
+One-chunk tiles serve smaller tables; each tiny case is a small ragged table,
+checked in full."""
 import pytest
 import torch
 
@@ -49,8 +52,32 @@ def test_long_tile_kernel(opt, rho_bits, fp32_grad, v_nonzero):
     torch.cuda.empty_cache()
 
 
+MID = [4 * 1024 * 1024 + 4097, 999, 1024 * 1024 + 33, 65536, 777777]
+
+
 @pytest.mark.parametrize("opt,rho_bits,fp32_grad,v_nonzero", CASES)
 def test_short_tile_kernel(opt, rho_bits, fp32_grad, v_nonzero):
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(rho_bits * 5 + fp32_grad * 3 + v_nonzero + 7)
+    dev = []
+    for n in MID:
+        d = fo.CompressedTensor(n, "cuda", rho_bits, opt == "adamw", 0.01)
+        d.init_from(torch.randn(n, device="cuda", generator=gen) * 0.02)
+        dev.append(d)
+    hp = dict(HP[opt], v_nonzero=v_nonzero) if opt == "adamw" else HP[opt]
+    samples = _samples_of(MID, per_row=1 << 15)
+    launches = fo.fo_kernel_launch_count()
+    for t in (1, 2):
+        g = [torch.randn(n, device="cuda", generator=gen) * 1e-3 for n in MID]
+        g = g if fp32_grad else [x.to(torch.bfloat16) for x in g]
+        _sampled_parity(opt, dev, g, samples, t, hp)
+    assert fo.fo_kernel_launch_count() - launches == 2
+    del dev
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("opt,rho_bits,fp32_grad,v_nonzero", CASES)
+def test_tiny_tile_kernel(opt, rho_bits, fp32_grad, v_nonzero):
     rng = np.random.default_rng(rho_bits * 7 + fp32_grad * 3 + v_nonzero + 100)
     thetas = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in RAGGED]
 
