@@ -189,37 +189,49 @@ class _FlashOptimizer(torch.optim.Optimizer):
         producing; ``bucket_numel=0`` steps each parameter on its own. Returns
         the hook handles."""
         handles = []
-        groups = {id(p): g for g in self.param_groups for p in g["params"]}
         wanted = None if params is None else {id(p) for p in params}
-        pending: Dict[int, list] = {}        # id(group) -> [group, params, numel]
         queued = [False]
 
-        def flush(gid: int) -> None:
-            group, ps, _ = pending.pop(gid)
+        class Bucket:
+            __slots__ = ("group", "params", "numel")
+
+            def __init__(self, group):
+                self.group, self.params, self.numel = group, [], 0
+
+        buckets: List[Bucket] = []
+
+        def flush(b: Bucket) -> None:
+            ps, b.params, b.numel = b.params, [], 0
             with torch.no_grad():
-                self._step_params(ps, group)
+                self._step_params(ps, b.group)
             for q in ps:
                 q.grad = None
 
         def flush_all() -> None:
             queued[0] = False
-            for gid in list(pending):
-                flush(gid)
+            for b in buckets:
+                if b.params:
+                    flush(b)
 
         self._release_flush = flush_all
-        for p_id, group in groups.items():
+        seen = set()
+        for group in self.param_groups:
             if not group["compress"]:
                 continue
+            bucket = Bucket(group)
+            buckets.append(bucket)
             for p in group["params"]:
-                if id(p) != p_id or (wanted is not None and p_id not in wanted):
+                if id(p) in seen or (wanted is not None and id(p) not in wanted):
                     continue
+                seen.add(id(p))
 
-                def hook(param, group=group):
-                    entry = pending.setdefault(id(group), [group, [], 0])
-                    entry[1].append(param)
-                    entry[2] += param.numel()
-                    if entry[2] >= bucket_numel:
-                        flush(id(group))
+                # per call: two attribute updates and a compare; the bucket
+                # and the element count are bound when the hook is made
+                def hook(param, b=bucket, n=p.numel()):
+                    b.params.append(param)
+                    b.numel += n
+                    if b.numel >= bucket_numel:
+                        flush(b)
                     elif not queued[0]:
                         # the rest of the bucket is stepped when this backward pass ends
                         torch.autograd.Variable._execution_engine.queue_callback(flush_all)
