@@ -297,7 +297,8 @@ def _gpu_id_for_smi(device_index: int) -> str:
 # stored per parameter (see record_traffic); valid while the sources hash to
 # the captured version.
 TRAFFIC = os.path.join(ROOT, "profiles", "fo_fused_step_kernel_traffic.json")
-STEP_SOURCES = ("fo_api.cu", "fo_device.cuh", "fo_internal.h", "fo_pair.cuh", "fo_step.cu")
+STEP_SOURCES = ("fo_api.cu", "fo_device.cuh", "fo_internal.h", "fo_pair.cuh", "fo_step.cu", "fo_step.cuh",
+                "fo_step_adamw.cu", "fo_step_adamw_dev.cu", "fo_step_sgd.cu", "fo_step_lion.cu")
 
 
 def _kernel_source_hash() -> str:

@@ -220,6 +220,25 @@ fo_status_t fo_adamw_step(const fo_tensor_t *table, int32_t ntensors,
                           const fo_adamw_hparams_t *hp, int64_t step, fo_stream_t stream);
 
 /*
+ * fo_adamw_step_dev -- fo_adamw_step with the step counter t read from
+ * DEVICE memory when the kernel runs: step_dev points to one int64_t
+ * (8-byte aligned, caller-owned) on the current device. The bias corrections
+ * and the other step-dependent scalars are then derived on the device, with
+ * the same double-precision expressions as fo_adamw_step, so the two calls
+ * give identical results for the same t. This serves steps captured in a
+ * CUDA graph: a replay reads the counter's value at that moment, where
+ * fo_adamw_step would repeat the t it was captured with. The call does not
+ * advance the counter; the caller does (for example with an increment
+ * enqueued, or captured, before the call). If the counter holds a value below
+ * 1 when the kernel runs, the launch updates nothing.
+ * Errors: those of fo_adamw_step (without the step check), FO_ERR_NULL
+ * (step_dev), FO_ERR_MISALIGNED (step_dev not 8-byte aligned).
+ */
+fo_status_t fo_adamw_step_dev(const fo_tensor_t *table, int32_t ntensors,
+                              const fo_adamw_hparams_t *hp, const int64_t *step_dev,
+                              fo_stream_t stream);
+
+/*
  * fo_sgd_step -- one fused FlashSGD step (SGD with momentum and the same
  * compression; pages' sections "论文背景和研究动机" and "融合优化器步骤").
  * Rows need theta, rho, m_q, m_scale, grad; v_q and v_scale are ignored.

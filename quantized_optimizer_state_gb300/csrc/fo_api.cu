@@ -260,7 +260,7 @@ void set_range(fo::StepScalars &s, float lo, float hi)
     s.hi = std::nextafter(hi, 0.0f);
 }
 
-// AdamW's packed fast path (fo_step.cu, pair_fast) divides and takes square
+// AdamW's packed fast path (fo_step.cuh, pair_fast) divides and takes square
 // roots with sequences validated for operands in [2^-100, 2^100] (and zero
 // numerators). With the per-element check that the gradient g is 0 or
 // T <= |g| <= 2^24, these conditions keep every operand inside:
@@ -277,13 +277,16 @@ void set_range(fo::StepScalars &s, float lo, float hi)
 // Then m' = 2^32 m and m'/den lie in [2^-100, 2^100] or are zero (a large
 // gradient also makes den large), and phi_m's quotient too. Calls outside
 // these conditions take the IEEE path throughout.
-void adamw_fast_ranges(fo::StepScalars &s)
+// t_known: the step scalars a[5], a[6] are set (fo_adamw_step); otherwise
+// (fo_adamw_step_dev) the kernel adds their conditions on the device.
+void adamw_fast_ranges(fo::StepScalars &s, bool t_known)
 {
     const float b1 = s.a[0], b2 = s.a[1], c1 = s.a[2], c2 = s.a[3], step = -s.a[5];
-    bool fast = s.a[4] >= 0x1p-40f && s.a[4] <= 0x1p20f && s.a[6] <= 0x1p8f;
+    bool fast = s.a[4] >= 0x1p-40f && s.a[4] <= 0x1p20f;
     fast = fast && (b1 == 0.0f || b1 >= 0x1p-16f) && (b2 == 0.0f || b2 >= 0x1p-16f);
     fast = fast && c1 >= 0x1p-24f && c2 >= 0x1p-24f;
-    fast = fast && (step == 0.0f || step >= 0x1p-80f);
+    if (t_known)
+        fast = fast && s.a[6] <= 0x1p8f && (step == 0.0f || step >= 0x1p-80f);
     double t = 0x1p-100;
     while (t < 0x1p-30 && !((double)c1 * t >= 0x1p-96 && (double)c2 * t * t >= 0x1p-98))
         t *= 2.0;
@@ -337,6 +340,31 @@ bool codec_aliases(int nin, const void *const *ptr, const int64_t *bytes, int co
             if ((a >= nin || b >= nin) && overlap(ptr[a], bytes[a], ptr[b], bytes[b]))
                 return true;
     return false;
+}
+
+// The step-independent part of AdamW's per-step scalars (the argument checks
+// and everything but the bias corrections), shared by both AdamW entry points.
+fo_status_t adamw_scalars(const fo_adamw_hparams_t *hp, fo::StepScalars &s)
+{
+    if (!hp)
+        return FO_ERR_NULL;
+    if (!is_finite(hp->lr) || hp->lr < 0.0 || !beta_ok(hp->beta1) || !beta_ok(hp->beta2) || !is_finite(hp->eps) ||
+        hp->eps <= 0.0 || (hp->flags & ~FO_ADAMW_V_NONZERO) != 0 || hp->reserved != 0)
+        return FO_ERR_BAD_ARG;
+    std::memset(&s, 0, sizeof s);
+    s.a[0] = (float)hp->beta1;
+    s.a[1] = (float)hp->beta2;
+    s.a[2] = (float)(1.0 - hp->beta1);
+    s.a[3] = (float)(1.0 - hp->beta2);
+    s.a[4] = (float)hp->eps;
+    // the packed fast path carries m' = 2^32 m (exact scalings of the constants)
+    s.p[0] = lanes(s.a[0] * 0x1p32f);
+    s.p[1] = lanes(-s.a[1]);
+    s.p[2] = lanes(s.a[2] * 0x1p32f);
+    s.p[3] = lanes(-s.a[3]);
+    s.p[5] = lanes(-s.a[4]);
+    s.v_nonzero = (hp->flags & FO_ADAMW_V_NONZERO) ? 1 : 0;
+    return FO_OK;
 }
 
 }  // namespace
@@ -430,34 +458,40 @@ fo_status_t fo_dequant_state(const void *q, const uint16_t *scales, float *x, in
 fo_status_t fo_adamw_step(const fo_tensor_t *table, int32_t ntensors, const fo_adamw_hparams_t *hp, int64_t step,
                           fo_stream_t stream)
 {
-    if (!hp)
-        return FO_ERR_NULL;
+    fo::StepScalars s;
+    fo_status_t st = adamw_scalars(hp, s);
+    if (st != FO_OK)
+        return st;
     if (step < 1)
         return FO_ERR_SIZE;
-    if (!is_finite(hp->lr) || hp->lr < 0.0 || !beta_ok(hp->beta1) || !beta_ok(hp->beta2) || !is_finite(hp->eps) ||
-        hp->eps <= 0.0 || (hp->flags & ~FO_ADAMW_V_NONZERO) != 0 || hp->reserved != 0)
-        return FO_ERR_BAD_ARG;
     const double bc1 = 1.0 - pow_by_squaring(hp->beta1, step);
     const double bc2 = 1.0 - pow_by_squaring(hp->beta2, step);
-    fo::StepScalars s;
-    std::memset(&s, 0, sizeof s);
-    s.a[0] = (float)hp->beta1;
-    s.a[1] = (float)hp->beta2;
-    s.a[2] = (float)(1.0 - hp->beta1);
-    s.a[3] = (float)(1.0 - hp->beta2);
-    s.a[4] = (float)hp->eps;
     s.a[5] = -(float)(hp->lr / bc1);
     s.a[6] = (float)(1.0 / std::sqrt(bc2));
-    // the packed fast path carries m' = 2^32 m (exact scalings of the constants)
-    s.p[0] = lanes(s.a[0] * 0x1p32f);
-    s.p[1] = lanes(-s.a[1]);
-    s.p[2] = lanes(s.a[2] * 0x1p32f);
-    s.p[3] = lanes(-s.a[3]);
     s.p[4] = lanes(s.a[6]);
-    s.p[5] = lanes(-s.a[4]);
     s.p[6] = lanes(s.a[5] * 0x1p-32f);
-    adamw_fast_ranges(s);
-    s.v_nonzero = (hp->flags & FO_ADAMW_V_NONZERO) ? 1 : 0;
+    adamw_fast_ranges(s, true);
+    return run_table(Opt::kAdamW, table, ntensors, s, hp->lr, decay_coef, stream);
+}
+
+fo_status_t fo_adamw_step_dev(const fo_tensor_t *table, int32_t ntensors, const fo_adamw_hparams_t *hp,
+                              const int64_t *step_dev, fo_stream_t stream)
+{
+    fo::StepScalars s;
+    fo_status_t st = adamw_scalars(hp, s);
+    if (st != FO_OK)
+        return st;
+    if (!step_dev)
+        return FO_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(step_dev) & 7u)
+        return FO_ERR_MISALIGNED;
+    // the kernel reads t and derives the step scalars (with the expressions
+    // of fo_adamw_step above) and the t-dependent preconditions itself
+    s.step_dev = reinterpret_cast<const long long *>(step_dev);
+    s.lr = hp->lr;
+    s.beta1 = hp->beta1;
+    s.beta2 = hp->beta2;
+    adamw_fast_ranges(s, false);
     return run_table(Opt::kAdamW, table, ntensors, s, hp->lr, decay_coef, stream);
 }
 

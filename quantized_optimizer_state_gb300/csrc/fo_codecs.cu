@@ -2,7 +2,7 @@
 // Efficient Training": weight splitting and merging (section "权重复分裂",
 // Eq. 1-2) and companded group quantization of the optimizer state (section
 // "带压缩扩展的优化器状态量化", Algorithms 2-3). They initialise and export
-// the compressed state; the fused step (fo_step.cu) uses the same primitives.
+// the compressed state; the fused step (fo_step.cuh) uses the same primitives.
 //
 // Split and quant: a thread owns 16 contiguous elements, and a 32-element
 // group is a pair of adjacent lanes (quant combines their absmax with one

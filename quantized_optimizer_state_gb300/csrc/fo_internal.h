@@ -65,14 +65,22 @@ static_assert(sizeof(StepRow) == 72, "StepRow layout");
 // lo, hi: the fast path's range for its checked operand x (AdamW: the
 // gradient; SGD, Lion: the new momentum): x = 0 or lo' <= |x| <= hi', given
 // as the FP32 values just below lo' and hi' (the guard compares the float
-// below |x|, see Guard in fo_step.cu).
+// below |x|, see Guard in fo_step.cuh).
 // v_nonzero (AdamW): requantize v with no code 0 in a group with a non-zero scale.
+// step_dev (AdamW, may be null): the step counter t in device memory; when
+// set, the kernel derives a[5], a[6], p[4], p[6] and the t-dependent part of
+// `fast` from *step_dev, lr, beta1 and beta2 (the host leaves them unset),
+// and skips the launch (skip) for t < 1.
 struct StepScalars {
     float a[8];
     unsigned long long p[8];
     float lo, hi;
     int32_t fast;
     int32_t v_nonzero;
+    const long long *step_dev;
+    double lr, beta1, beta2;
+    int32_t skip;
+    int32_t pad;
 };
 
 // Rows per launch: the whole table of one launch travels in the kernel's

@@ -78,6 +78,7 @@ SIGNATURES = {
     "fo_quant_state": (ctypes.c_int, [_VP, _VP, _VP, _I64, ctypes.c_int, _VP]),
     "fo_dequant_state": (ctypes.c_int, [_VP, _VP, _VP, _I64, ctypes.c_int, _VP]),
     "fo_adamw_step": (ctypes.c_int, [_VP, _I32, _VP, _I64, _VP]),
+    "fo_adamw_step_dev": (ctypes.c_int, [_VP, _I32, _VP, _VP, _VP]),
     "fo_sgd_step": (ctypes.c_int, [_VP, _I32, _VP, _VP]),
     "fo_lion_step": (ctypes.c_int, [_VP, _I32, _VP, _VP]),
     "fo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -313,6 +314,18 @@ def fo_adamw_step(table: Table, lr: float, beta1: float, beta2: float, eps: floa
     hp = AdamWHparams(lr, beta1, beta2, eps, FO_ADAMW_V_NONZERO if v_nonzero else 0, 0)
     _check("fo_adamw_step", lib().fo_adamw_step(table.ptr, table.n, ctypes.addressof(hp), int(step),
                                                 _stream(stream)))
+
+
+def fo_adamw_step_dev(table: Table, lr: float, beta1: float, beta2: float, eps: float, step,
+                      stream=None, v_nonzero: bool = False):
+    """AdamW with the step counter read on the device when the kernel runs:
+    ``step`` is a one-element int64 CUDA tensor (or a raw device address). For
+    steps captured in a CUDA graph; the caller advances the counter."""
+    hp = AdamWHparams(lr, beta1, beta2, eps, FO_ADAMW_V_NONZERO if v_nonzero else 0, 0)
+    import torch
+    ptr = _ptr(step, "step", (torch.int64,), 1)
+    _check("fo_adamw_step_dev", lib().fo_adamw_step_dev(table.ptr, table.n, ctypes.addressof(hp), ptr,
+                                                        _stream(stream)))
 
 
 def fo_sgd_step(table: Table, lr: float, momentum: float, stream=None):

@@ -80,13 +80,24 @@ class _FlashOptimizer(torch.optim.Optimizer):
             raise TypeError("parameters must be float32 (split on first use) or bfloat16")
         ng = (n + _GROUP - 1) // _GROUP
         st = self.state[p]
-        st["step"] = 0          # a Python int: the step counter t of this parameter
+        if group.get("capturable"):
+            st["step"] = self._group_counter(group, p.device)   # shared int64 device tensor
+        else:
+            st["step"] = 0      # a Python int: the step counter t of this parameter
         st["rho"] = rho
         st["m_q"] = torch.zeros(n, dtype=torch.int8, device=p.device)
         st["m_scale"] = torch.zeros(ng, dtype=torch.int16, device=p.device)
         if self._with_v:
             st["v_q"] = torch.zeros(n, dtype=torch.uint8, device=p.device)
             st["v_scale"] = torch.zeros(ng, dtype=torch.int16, device=p.device)
+
+    def _group_counter(self, group: Dict, device) -> torch.Tensor:
+        """The device step counter of a capturable group's parameters on `device`."""
+        counters = self.__dict__.setdefault("_counters", {})
+        key = (id(group), torch.device(device).index)
+        if key not in counters:
+            counters[key] = torch.zeros((), dtype=torch.int64, device=device)
+        return counters[key]
 
     def _make_reference(self, group: Dict) -> torch.optim.Optimizer:
         hp = {k: v for k, v in group.items() if k not in ("params", "rho_bits", "compress", "v_nonzero")}
@@ -153,6 +164,9 @@ class _FlashOptimizer(torch.optim.Optimizer):
             return
         # parameters of a group on the same device that have taken the same
         # number of steps share a call (a launch only touches its own device)
+        if group.get("capturable"):
+            self._step_params_capturable(params, group)
+            return
         by_key: Dict[tuple, List[torch.Tensor]] = {}
         for p in params:
             by_key.setdefault((int(self.state[p]["step"]) + 1, p.device.index), []).append(p)
@@ -170,7 +184,32 @@ class _FlashOptimizer(torch.optim.Optimizer):
             for p in ps:
                 self.state[p]["step"] = t
 
+    def _step_params_capturable(self, params: List[torch.Tensor], group: Dict) -> None:
+        """Capturable groups (FlashAdamW): the step counter is a device tensor
+        shared by the group's parameters on one device, advanced on the device
+        and read by the kernel, so the step can be captured in a CUDA graph and
+        replayed with the bias corrections moving on."""
+        by_dev: Dict[int, List[torch.Tensor]] = {}
+        for p in params:
+            by_dev.setdefault(p.device.index, []).append(p)
+        for dev, ps in by_dev.items():
+            counter = self.state[ps[0]]["step"]
+            grads = [self._grad_of(p) for p in ps]
+            with torch.cuda.device(dev):
+                table = self._table(ps, grads, group)
+                counter.add_(1)
+                try:
+                    self._launch_dev(table, group, counter)
+                except fo.FoError:
+                    counter.sub_(1)       # a refused call leaves the counter as it was
+                    raise
+                finally:
+                    table.release()
+
     def _launch(self, table: fo.Table, group: Dict, t: int) -> None:
+        raise NotImplementedError
+
+    def _launch_dev(self, table: fo.Table, group: Dict, counter: torch.Tensor) -> None:
         raise NotImplementedError
 
     # -- gradient release ---------------------------------------------------
@@ -270,9 +309,19 @@ class _FlashOptimizer(torch.optim.Optimizer):
                 if cur is not None and (cur.dtype != v.dtype or cur.shape != v.shape):
                     raise ValueError(f"state '{n}' does not match the parameter's layout")
                 self.state[p][n] = v.to(device=p.device).clone()
-        for st in self.state.values():
-            if "step" in st:
-                st["step"] = int(st["step"])    # checkpoints may hold it as a tensor
+        self.__dict__.pop("_counters", None)
+        for group in self.param_groups:
+            for p in group["params"]:
+                st = self.state.get(p)
+                if not st or "step" not in st:
+                    continue
+                if group.get("capturable"):
+                    # one counter per group and device again, holding the saved count
+                    c = self._group_counter(group, p.device)
+                    c.fill_(int(st["step"]))
+                    st["step"] = c
+                else:
+                    st["step"] = int(st["step"])    # checkpoints may hold it as a tensor
         self._tables.clear()
 
     # -- export ---------------------------------------------------------------
@@ -306,15 +355,24 @@ class FlashAdamW(_FlashOptimizer):
 
     v_nonzero=True opts into a rule the page does not have: a non-zero second
     moment is never stored as code 0, which would decode it to 0 and let the
-    momentum drive an update of about lr*m/eps."""
+    momentum drive an update of about lr*m/eps.
+
+    capturable=True keeps each group's step counter in device memory (one
+    int64 tensor shared by the group's parameters on a device, advanced on the
+    device by every step()), so that step() can be captured in a CUDA graph:
+    each replay advances the counter and the kernel derives the bias
+    corrections from it. Every parameter of such a group with a gradient is
+    stepped with the group's count (a parameter without a gradient at some
+    step is skipped, but the count moves on)."""
     _kind = "adamw"
     _with_v = True
     _reference = torch.optim.AdamW
 
     def __init__(self, params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01,
-                 rho_bits=8, compress=True, v_nonzero=False):
+                 rho_bits=8, compress=True, v_nonzero=False, capturable=False):
         super().__init__(params, dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay,
-                                      rho_bits=rho_bits, compress=compress, v_nonzero=v_nonzero))
+                                      rho_bits=rho_bits, compress=compress, v_nonzero=v_nonzero,
+                                      capturable=capturable))
 
     @staticmethod
     def _reference_args(hp):
@@ -324,6 +382,11 @@ class FlashAdamW(_FlashOptimizer):
         b1, b2 = group["betas"]
         fo.fo_adamw_step(table, group["lr"], b1, b2, group["eps"], t,
                          v_nonzero=bool(group.get("v_nonzero", False)))
+
+    def _launch_dev(self, table, group, counter):
+        b1, b2 = group["betas"]
+        fo.fo_adamw_step_dev(table, group["lr"], b1, b2, group["eps"], counter,
+                             v_nonzero=bool(group.get("v_nonzero", False)))
 
 
 class FlashSGD(_FlashOptimizer):

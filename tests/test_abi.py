@@ -252,3 +252,18 @@ def test_table_keeps_its_tensors_alive(monkeypatch):
     t.release()
     gc.collect()
     assert ref() is None
+
+
+def test_adamw_step_dev_argument_errors():
+    """The device-counter AdamW call checks its hyper-parameters, the counter's
+    address and the table on the host, before anything is launched."""
+    hp = fo.AdamWHparams(1e-3, 0.9, 0.999, 1e-8)
+    bad_hp = fo.AdamWHparams(1e-3, 1.0, 0.999, 1e-8)
+    rows = (fo.FoTensor * 1)(_table(rho_bits=3))          # an invalid row: never launches
+    A = 1 << 20
+    assert _call("fo_adamw_step_dev", ctypes.addressof(rows), 1, ctypes.addressof(hp), None, None) == 1
+    assert _call("fo_adamw_step_dev", ctypes.addressof(rows), 1, ctypes.addressof(hp), A + 4, None) == 2
+    assert _call("fo_adamw_step_dev", ctypes.addressof(rows), 1, ctypes.addressof(bad_hp), A, None) == 4
+    assert _call("fo_adamw_step_dev", ctypes.addressof(rows), 1, None, A, None) == 1
+    assert _call("fo_adamw_step_dev", ctypes.addressof(rows), 1, ctypes.addressof(hp), A, None) == 4   # the row
+    assert _call("fo_adamw_step_dev", None, 0, ctypes.addressof(hp), A, None) == 0                      # empty table
