@@ -169,3 +169,28 @@ def test_capturable_flash_adamw_matches_and_replays():
             assert torch.equal(oa.state[x][k], ob.state[y][k])
             assert torch.equal(oa.state[x][k], oc.state[z][k])
     assert int(ob.state[pb[0]]["step"].item()) == 5 and int(oc.state[pc[0]]["step"].item()) == 5
+
+
+@pytest.mark.parametrize("n", [6 * 1024 * 1024 + 77, 1 << 27])
+def test_device_counter_on_long_and_short_tiles(n):
+    """The device-counter kernels of the other two tile lengths (a table of a
+    few million elements takes 2-chunk tiles, one of 2^27 8-chunk tiles):
+    identical to the host-counter call."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(n % 1000)
+    a = fo.CompressedTensor(n, "cuda", 8, True, 0.01)
+    a.init_from(torch.randn(n, device="cuda", generator=gen) * 0.02)
+    b = fo.CompressedTensor(n, "cuda", 8, True, 0.01)
+    for x, y in zip(b.buffers(), a.buffers()):
+        x.copy_(y)
+    counter = torch.zeros((), dtype=torch.int64, device="cuda")
+    for t in (1, 2, 3):
+        g = (torch.randn(n, device="cuda", generator=gen) * 1e-3).to(torch.bfloat16)
+        fo.fo_adamw_step(fo.table_of([a], [g]), 1e-3, 0.9, 0.999, 1e-8, t)
+        counter.fill_(t)
+        fo.fo_adamw_step_dev(fo.table_of([b], [g]), 1e-3, 0.9, 0.999, 1e-8, counter)
+    torch.cuda.synchronize()
+    for x, y in zip(a.buffers(), b.buffers()):
+        assert torch.equal(x, y)
+    del a, b
+    torch.cuda.empty_cache()
