@@ -255,6 +255,32 @@ fo_status_t fo_sgd_step(const fo_tensor_t *table, int32_t ntensors, const fo_sgd
 fo_status_t fo_lion_step(const fo_tensor_t *table, int32_t ntensors,
                          const fo_lion_hparams_t *hp, fo_stream_t stream);
 
+/*
+ * fo_verify_fast_arithmetic -- the fused step (section "融合优化器步骤")
+ * must leave exactly the state the IEEE operations of the contract above
+ * give. Its fast path builds division and square root from the GPU's
+ * reciprocal and reciprocal-square-root approximations, whose exact results
+ * the instruction set leaves open; each sequence is exact on a one-variable
+ * or finite operand domain given the approximation's behaviour. This call
+ * enumerates every such domain on the CURRENT device, running the step's own
+ * device functions, and counts the operands whose result differs from the
+ * IEEE operation (both signs where the domain is signed):
+ *   counts[0]  refined reciprocal vs RN(1/b), every b in [2^-100, 2^100]
+ *   counts[1]  square root vs RN(sqrt(v)), every v in [2^-100, 2^126] and 0
+ *   counts[2]  phi_m division of AdamW (m scaled by 2^32), every |m'| in
+ *              [2^-62, 2^85]
+ *   counts[3]  phi_m division of SGD and Lion, every |m| in [2^-100, 2^100]
+ *   counts[4]  momentum decoding phi_m^-1(code * s/127), every code byte
+ *              under every FP16 scale below 127/64
+ *   counts[5]  127/s, 255/s, s/127 and s/255, every positive finite FP16 s
+ * All are 0 where the fast path is exact. `counts`: DEVICE memory of
+ * FO_VERIFY_COUNTS uint64 entries (8-byte aligned) owned by the caller,
+ * overwritten; the work (about 7e9 evaluations) is enqueued on `stream`.
+ * Errors: FO_ERR_NULL, FO_ERR_MISALIGNED, FO_ERR_CUDA.
+ */
+#define FO_VERIFY_COUNTS 6
+fo_status_t fo_verify_fast_arithmetic(uint64_t *counts, fo_stream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char *fo_status_string(fo_status_t status);
 

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libfo.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["fo_api.cu", "fo_step.cu", "fo_step_adamw.cu", "fo_step_adamw_dev.cu", "fo_step_sgd.cu",
-           "fo_step_lion.cu", "fo_codecs.cu"]
+           "fo_step_lion.cu", "fo_codecs.cu", "fo_verify.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # -Xcompiler -ffp-contract=off: the host code derives the per-step scalars in
 # double (1 - lr*wd and so on), which the contract defines as separately

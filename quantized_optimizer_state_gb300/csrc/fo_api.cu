@@ -548,6 +548,19 @@ const char *fo_status_string(fo_status_t status)
     return "unknown fo_status_t";
 }
 
+fo_status_t fo_verify_fast_arithmetic(uint64_t *counts, fo_stream_t stream)
+{
+    if (!counts)
+        return FO_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(counts) & 7u) != 0)
+        return FO_ERR_MISALIGNED;
+    fo_status_t st = pending_error();
+    if (st != FO_OK)
+        return st;
+    return cuda_status(fo::launch_verify(reinterpret_cast<unsigned long long *>(counts),
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 int fo_last_cuda_error(void) { return fo::t_last_cuda_error; }
 
 uint64_t fo_kernel_launch_count(void) { return fo::g_launches.load(std::memory_order_relaxed); }

@@ -329,15 +329,15 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(const void *__restric
             float x[4];
             if (Kind == 0 && small_scale) {
                 // phi_m^-1(z) = z / (2 - |z|) on element pairs, |z| < 2: the
-                // divisor lies in [2^-23, 2] and the quotient is 0 or at least
-                // 2^-33 in magnitude (|z| >= 2^-24/127), inside the validated
-                // range of div2 (the correctly rounded division of fo_pair.cuh)
+                // short division of fo_pair.cuh, enumerated equal to the IEEE
+                // division for every code byte under every scale 0x0000-0x3FEF
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const f2 d = mul2(pk(cc[2 * h], cc[2 * h + 1]), splat(step));
                     float d0, d1;
                     unpk(d, d0, d1);
-                    unpk(div2(d, pk(__fsub_rn(fabsf(d0), 2.0f), __fsub_rn(fabsf(d1), 2.0f))), x[2 * h], x[2 * h + 1]);
+                    unpk(div2_short(d, pk(__fsub_rn(fabsf(d0), 2.0f), __fsub_rn(fabsf(d1), 2.0f))), x[2 * h],
+                         x[2 * h + 1]);
                 }
             } else {
 #pragma unroll

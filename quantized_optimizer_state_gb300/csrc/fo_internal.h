@@ -112,6 +112,11 @@ cudaError_t launch_quant(const float *x, void *q, uint16_t *scales, int64_t n, i
 cudaError_t launch_dequant(const void *q, const uint16_t *scales, float *x, int64_t n, int kind,
                            cudaStream_t stream);
 
+// On-device enumeration of the fast path's hardware-dependent arithmetic
+// (fo_verify.cu): kVerifyCounts mismatch counts written to `counts` (device).
+constexpr int kVerifyCounts = 6;
+cudaError_t launch_verify(unsigned long long *counts, cudaStream_t stream);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 // Kernel launches issued by this library so far.

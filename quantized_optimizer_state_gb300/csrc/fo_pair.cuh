@@ -14,13 +14,24 @@
 // reciprocal-square-root approximation y, the exact remainder d = v - s*s
 // and RN(s + d*h) (the same remainder correction, for square roots).
 //
-// Validity: both sequences were checked bit for bit against the CUDA
-// correctly rounded operations -- the reciprocal over every significand of
-// ten binades from 2^-126 to 2^125, the division over 3.2e9 operand pairs,
-// the square root over every FP32 value from 2^-100 up.
-// They are used only where the operands are inside the ranges listed at each
-// function; callers check the ranges and recompute elsewhere with the IEEE
-// operations.
+// Short division (div2_short, div1_short): the same correction on the
+// unrefined approximation y0, RN(q0 + r*y0) with q0 = RN(a*y0). y0 is not
+// always RN(1/b) (it differs for 13 % of the FP32 values of b), and over all
+// 2^46 pairs of significands this sequence misses RN(a/b) 79,381 times, so it
+// serves only domains on which it was enumerated exhaustively and found equal
+// to the IEEE division: phi_m's divisions (every m in the fast path's range),
+// the momentum dequantization (every code byte under every fast-path scale)
+// and the code multipliers 127/s and 255/s (every positive finite FP16 s).
+//
+// Validity: the hardware approximations are facts of the GPU, not of the
+// instruction set, so fo_verify_fast_arithmetic (fo_verify.cu) re-enumerates,
+// on the device at hand, every one-variable or finite domain the fast path
+// relies on: the refined reciprocal equal to RN(1/b) for every b in
+// [2^-100, 2^100] (the premise of Markstein's theorem for div2), the short
+// division on the domains above, and the square root for every v in
+// [2^-100, 2^126] and v = 0. The sequences are used only where the operands
+// are inside the ranges listed at each function; callers check the ranges
+// and recompute elsewhere with the IEEE operations.
 #pragma once
 
 #include <cstdint>
@@ -86,33 +97,33 @@ __device__ __forceinline__ float rsqrt_approx(float x)
     return y;
 }
 
-// RN(a / b) in both lanes, given nb = -b. Valid when b is in [2^-100, 2^100],
-// a is +0 or has |a| >= 2^-100, and the quotient is in [2^-100, 2^100] or 0;
-// also for any a when b is 1/2 or 1 exactly (the refined reciprocal is then
-// exactly 1/b, q0 = a/b exactly and the remainder is 0). q0 (the first
-// quotient) is returned for range checks.
-__device__ __forceinline__ f2 div2(f2 a, f2 nb, f2 &q0)
+// RN(1/b) in both lanes, given nb = -b with b in [2^-100, 2^100]: one
+// Newton step y0 + y0*(1 - b*y0) on the hardware approximation y0
+// (enumerated over that whole range).
+__device__ __forceinline__ f2 rcp2_rn(f2 nb)
 {
     float n0, n1;
     unpk(nb, n0, n1);
     const f2 y0 = pk(rcp_approx(-n0), rcp_approx(-n1));
     const f2 e = fma2(nb, y0, splat(1.0f));  // 1 - b*y0
-    const f2 y1 = fma2(y0, e, y0);            // RN(1/b)
-    q0 = mul2(a, y1);
+    return fma2(y0, e, y0);
+}
+
+// RN(a / b) in both lanes, given nb = -b. Valid when b is in [2^-100, 2^100],
+// a is +0 or has |a| >= 2^-100, and the quotient is in [2^-100, 2^100] or 0
+// (Markstein's theorem, given the correctly rounded reciprocal).
+__device__ __forceinline__ f2 div2(f2 a, f2 nb)
+{
+    const f2 y1 = rcp2_rn(nb);                // RN(1/b)
+    const f2 q0 = mul2(a, y1);
     const f2 r = fma2(nb, q0, a);             // a - b*q0, exact
     return fma2(r, y1, q0);
 }
 
-__device__ __forceinline__ f2 div2(f2 a, f2 nb)
-{
-    f2 q0;
-    return div2(a, nb, q0);
-}
-
 // -RN(sqrt(v)) in both lanes, given nv = -v with v in [2^-100, 2^126]:
 // s = v*y and h = y/2 from the hardware reciprocal square root y, then the
-// exact remainder d = v - s*s and RN(s + d*h) (checked equal to __fsqrt_rn
-// for every FP32 in [2^-100, 2^128)). Also v = +0 (nv = -0), for which the
+// exact remainder d = v - s*s and RN(s + d*h) (enumerated equal to the IEEE
+// square root over that whole range). Also v = +0 (nv = -0), for which the
 // result is +0: the approximation reads v + 2^-126, which is v itself for
 // every v >= 2^-100 (2^-126 is below half an ulp there) and a normal number
 // for v = 0, so that y stays finite and s = -0 * y, d and the result are
@@ -128,6 +139,30 @@ __device__ __forceinline__ f2 neg_sqrt2(f2 nv)
     return fma2(d, h, ns);                    // -(s + (v - s*s)*h)
 }
 
+// RN(a / b) in both lanes, given nb = -b, by the short sequence (no
+// refinement of the reciprocal approximation). Exact only on the enumerated
+// domains listed at the top of this file; for a = -0 it returns +0 (as div2
+// does), where callers rely on the value only.
+__device__ __forceinline__ f2 div2_short(f2 a, f2 nb)
+{
+    float n0, n1;
+    unpk(nb, n0, n1);
+    const f2 y0 = pk(rcp_approx(-n0), rcp_approx(-n1));
+    const f2 q0 = mul2(a, y0);
+    const f2 r = fma2(nb, q0, a);             // a - b*q0, exact
+    return fma2(r, y0, q0);
+}
+
+// RN(a / s) by the short sequence, for a = 127 or 255 and s a positive
+// finite FP16 value (enumerated).
+__device__ __forceinline__ float div1_short(float a, float s)
+{
+    const float y0 = rcp_approx(s);
+    const float q0 = __fmul_rn(a, y0);
+    const float r = __fmaf_rn(-s, q0, a);
+    return __fmaf_rn(r, y0, q0);
+}
+
 // RN(a / b) for a constant b with its correctly rounded reciprocal y = RN(1/b)
 // (Markstein's correction step only), valid for a = 0 or |a/b| in
 // [2^-100, 2^100] with a normal.
@@ -138,15 +173,5 @@ __device__ __forceinline__ float div_by_const(float a, float nb, float y)
     return __fmaf_rn(r, y, q0);
 }
 
-// RN(a / b) for a scalar b in [2^-100, 2^100] and a/b in the same range.
-__device__ __forceinline__ float div1(float a, float b)
-{
-    const float y0 = rcp_approx(b);
-    const float e = __fmaf_rn(-b, y0, 1.0f);
-    const float y1 = __fmaf_rn(y0, e, y0);
-    const float q0 = __fmul_rn(a, y1);
-    const float r = __fmaf_rn(-b, q0, a);
-    return __fmaf_rn(r, y1, q0);
-}
 
 }  // namespace fo

@@ -209,7 +209,12 @@ __device__ __forceinline__ void element_exact(const Loaded &L, const uint32_t (&
         nr_out = 0.0f;
     }
     theta_out = theta;
-    z_out = __fmul_rn(phi_m(m), ZScale<O>::up);
+    // an infinite momentum (a code byte of -128 decodes to -inf under the
+    // scale 127/64) companded is NaN: coded 0 like any NaN, which a zero z
+    // gives, and left out of the group maximum (fmaxf ignores NaN and 0 does
+    // not raise it)
+    const float zz = __fmul_rn(phi_m(m), ZScale<O>::up);
+    z_out = zz != zz ? 0.0f : zz;
 }
 
 template <Opt O, int RB, int GB, int... J>
@@ -331,8 +336,9 @@ __device__ __forceinline__ f2 mhat_pair(const uint32_t (&mx)[4], const PairConst
     const f2 zq = mul2(q, k.cm);
     float a0, a1;
     unpk(zq, a0, a1);
-    // |zq| - 2 = -(2 - |zq|): the operands are below 2 in magnitude (scale < 2)
-    return div2(zq, pk(__fsub_rn(fabsf(a0), 2.0f), __fsub_rn(fabsf(a1), 2.0f)));
+    // |zq| - 2 = -(2 - |zq|): |zq| < 2 for every code byte (-128 included)
+    // under the fast path's momentum scales (below 127/64, see thread_step)
+    return div2_short(zq, pk(__fsub_rn(fabsf(a0), 2.0f), __fsub_rn(fabsf(a1), 2.0f)));   // enumerated domain
 }
 
 // z = phi_m(m) = RN(2m / RN(1 + |m|)), packed, as RN(m / (RN(1 + |m|)/2)):
@@ -347,7 +353,8 @@ __device__ __forceinline__ f2 phi_m_pair(f2 m)
     constexpr float kHalfOverZ = ZS == 1 ? -0.5f : -0x1p-33f;
     float m0, m1;
     unpk(m, m0, m1);
-    return div2(m, pk(__fmaf_rn(kHalfOverZ, fabsf(m0), -0.5f), __fmaf_rn(kHalfOverZ, fabsf(m1), -0.5f)));
+    // (the short division: enumerated over every m of the fast path's range)
+    return div2_short(m, pk(__fmaf_rn(kHalfOverZ, fabsf(m0), -0.5f), __fmaf_rn(kHalfOverZ, fabsf(m1), -0.5f)));
 }
 
 template <Opt O, int RB, int GB, int W>
@@ -449,12 +456,14 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
     float th[kEPT], z[kEPT], nr[kEPT];
     float av = 0.0f;   // the thread's largest sqrt(v) (AdamW)
     // the fast path needs the host's range preconditions and a momentum scale
-    // below 2 (so that 2 - |z| stays positive); otherwise every element of
-    // this thread goes through the exact path
-    // (an FP16 pattern of 0x4000 or more is 2.0 or above, infinite, NaN or
-    // negative). AdamW and Lion also need a decay factor of at least 2^-8 in
-    // magnitude, so that a decayed theta is never zero.
-    bool bad = !s.fast || L.ms >= 0x4000u || (O != Opt::kSgd && !(fabsf(row.coef) >= 0x1p-8f));
+    // s below 127/64 = 1.984375, where |z| = |q| s/127 < 2 for every code
+    // byte q (-128 included, which the quantizer never writes but a caller
+    // may pass), so that 2 - |z| stays positive; otherwise every element of
+    // this thread goes through the exact path (an FP16 pattern of 0x3FF0 or
+    // more is 127/64 or above, infinite, NaN or negative). AdamW and Lion also
+    // need a decay factor of at least 2^-8 in magnitude, so that a decayed
+    // theta is never zero.
+    bool bad = !s.fast || L.ms >= 0x3FF0u || (O != Opt::kSgd && !(fabsf(row.coef) >= 0x1p-8f));
     if (!bad) {
         PairConsts k;
         k.cm = splat(cm);
@@ -533,13 +542,14 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
 
     const uint16_t sm_new = scale_of(__fmul_rn(am, ZScale<O>::down));   // exact: am is 2^32 |z| for AdamW
     const uint16_t sv_new = WithV ? scale_of(av) : (uint16_t)0;
-    // code multipliers 127/s (m) and 255/s (v), 0 for a zero scale; s is an
-    // FP16 value in [2^-24, 65504], inside the validated division range
+    // code multipliers 127/s (m) and 255/s (v), 0 for a zero scale; s is a
+    // positive finite FP16 value there, on which the short division was
+    // enumerated
     const float s_m = scale_value(sm_new), s_v = scale_value(sv_new);
     // (for AdamW z holds 2^32 z, so the multiplier is scaled by 2^-32: exact,
     // and the product z * (127/s) is the same real number)
-    const float mult_m = s_m > 0.0f ? __fmul_rn(div1(127.0f, s_m), ZScale<O>::down) : 0.0f;
-    const float mult_v = (WithV && s_v > 0.0f) ? div1(255.0f, s_v) : 0.0f;
+    const float mult_m = s_m > 0.0f ? __fmul_rn(div1_short(127.0f, s_m), ZScale<O>::down) : 0.0f;
+    const float mult_v = (WithV && s_v > 0.0f) ? div1_short(255.0f, s_v) : 0.0f;
     // codes: clamp(rint(x)), x = RN(phi * (L/s)). For m with a normal FP16
     // scale below the 65504 cap the group maximum is at most s*(1 + 2^-11),
     // so |x| <= 127.07: no clamp can apply, and rint is the magic-number

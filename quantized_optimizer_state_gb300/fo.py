@@ -81,6 +81,7 @@ SIGNATURES = {
     "fo_adamw_step_dev": (ctypes.c_int, [_VP, _I32, _VP, _VP, _VP]),
     "fo_sgd_step": (ctypes.c_int, [_VP, _I32, _VP, _VP]),
     "fo_lion_step": (ctypes.c_int, [_VP, _I32, _VP, _VP]),
+    "fo_verify_fast_arithmetic": (ctypes.c_int, [_VP, _VP]),
     "fo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fo_last_cuda_error": (ctypes.c_int, []),
     "fo_kernel_launch_count": (ctypes.c_uint64, []),
@@ -344,6 +345,27 @@ def fo_status_string(status: int) -> str:
 
 def fo_kernel_launch_count() -> int:
     return int(lib().fo_kernel_launch_count())
+
+
+FO_VERIFY_COUNTS = 6
+VERIFY_CHECKS = ("reciprocal", "square_root", "phi_m_adamw", "phi_m_sgd_lion", "momentum_decode",
+                 "scale_divisions")
+
+
+def fo_verify_fast_arithmetic(counts=None, stream=None) -> dict:
+    """Enumerate, on the current device, every operand domain on which the
+    fast path's division and square root depend on the GPU's approximations,
+    and return the mismatch count of each against the IEEE operation (all 0
+    where the fast path is exact). ``counts``: an optional int64 CUDA tensor of
+    FO_VERIFY_COUNTS elements to write into; the call waits for the result."""
+    import torch
+    if counts is None:
+        counts = torch.zeros(FO_VERIFY_COUNTS, dtype=torch.int64, device="cuda")
+    ptr = _ptr(counts, "counts", (torch.int64,), FO_VERIFY_COUNTS)
+    s = _stream(stream)
+    _check("fo_verify_fast_arithmetic", lib().fo_verify_fast_arithmetic(ptr, s))
+    torch.cuda.synchronize()
+    return dict(zip(VERIFY_CHECKS, (int(c) for c in counts.cpu().tolist())))
 
 
 # --- device-resident compressed state (torch tensors as memory) ---------------

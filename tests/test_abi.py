@@ -267,3 +267,9 @@ def test_adamw_step_dev_argument_errors():
     assert _call("fo_adamw_step_dev", ctypes.addressof(rows), 1, None, A, None) == 1
     assert _call("fo_adamw_step_dev", ctypes.addressof(rows), 1, ctypes.addressof(hp), A, None) == 4   # the row
     assert _call("fo_adamw_step_dev", None, 0, ctypes.addressof(hp), A, None) == 0                      # empty table
+
+
+def test_verify_fast_arithmetic_argument_errors():
+    A = 1 << 20
+    assert _call("fo_verify_fast_arithmetic", None, None) == 1          # FO_ERR_NULL
+    assert _call("fo_verify_fast_arithmetic", A + 4, None) == 2         # not 8-byte aligned

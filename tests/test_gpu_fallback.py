@@ -96,6 +96,20 @@ def test_momentum_scale_two_decodes_to_infinity():
     _step_and_compare("adamw", st, g, steps=1)
 
 
+@pytest.mark.parametrize("opt", ["adamw", "sgd", "lion"])
+def test_momentum_code_minus_128_near_scale_two(opt):
+    """A momentum byte of -128 (never written by the quantizer, but any byte
+    may be passed) under FP16 scales from 1.984375 = 127/64 up: there
+    |z| = 128 s/127 reaches 2, and at 127/64 exactly z = -2 and
+    phi_m^-1(z) = -2/0 = -inf. Scales just below stay on the fast path."""
+    rng, st, g = _base(8, opt == "adamw")
+    for grp, s in ((1, 0x3FF0), (2, 0x3FF1), (3, 0x3FFF), (4, 0x3FEF), (128, 0x3FF0)):
+        st.m_scale[grp] = s
+        st.m_q[32 * grp + 5] = -128
+        st.m_q[32 * grp + 6] = 127
+    _step_and_compare(opt, st, g, steps=1)
+
+
 def test_tiny_second_moment_and_tiny_quotients():
     rng, st, g = _base(4)
     g[200:232] = 0.0                     # v = 0 at step 1: exact path
