@@ -29,11 +29,16 @@ constexpr int kMinTilesPerCta = 8;
 
 enum class Opt : int { kAdamW = 0, kSgd = 1, kLion = 2 };
 
-// Resident CTAs per SM each step kernel is built for: AdamW needs 80
-// registers a thread for its fast path without spilling (3 CTAs of 256
-// threads); SGD and Lion, with one moment, fit in 64 (4 CTAs: more warps to
-// hide latency, 6 % faster on the Llama-3.1-8B Lion step than 3).
-constexpr int step_ctas_per_sm(Opt o) { return o == Opt::kAdamW ? 3 : 4; }
+// Resident CTAs per SM each step kernel is built for (256 threads each), by
+// measurement on the Llama-3.1-8B table. AdamW with 8-bit rho and BF16
+// gradients runs 4 (64 registers, a few bytes of spills: 16.7 against 17.5
+// ms at 3); with 16-bit rho or FP32 gradients, which hold 4 or 8 more words a
+// thread, 3 (80 registers: 18.4 against 18.9 ms at 4). SGD and Lion, with one
+// moment, run 4 (6 % faster on the Lion step than 3).
+constexpr int step_ctas_per_sm(Opt o, int rho_bits, int grad_bits)
+{
+    return o != Opt::kAdamW ? 4 : (rho_bits == 8 && grad_bits == 16 ? 4 : 3);
+}
 
 // One table row as the step kernel sees it. `coef` is the per-tensor scalar:
 // the decay factor (1 - lr*wd) for AdamW and Lion, the weight decay for SGD.
