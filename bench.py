@@ -722,6 +722,25 @@ def _link_rates(h_src, d_dst, d_src, h_dst, nbytes, stream_a, stream_b, device):
             "both_directions_gbs": 2 * nbytes / timed(both) / 1e9, "probe_bytes": nbytes}
 
 
+def _both_full_ms(h_src, d_dst, d_src, h_dst, piece, stream_a, stream_b, device):
+    """Milliseconds to copy the whole of h_src to d_dst and of d_src to h_dst at
+    once (two streams, pieces of `piece` elements interleaved): the end-to-end
+    leg's own copies with no compute, the floor of one end-to-end step."""
+    import torch
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    n_in, n_out = h_src.numel(), h_dst.numel()
+    for a in range(0, max(n_in, n_out), piece):
+        if a < n_in:
+            with torch.cuda.stream(stream_a):
+                d_dst[a:min(n_in, a + piece)].copy_(h_src[a:min(n_in, a + piece)], non_blocking=True)
+        if a < n_out:
+            with torch.cuda.stream(stream_b):
+                h_dst[a:min(n_out, a + piece)].copy_(d_src[a:min(n_out, a + piece)], non_blocking=True)
+    torch.cuda.synchronize(device)
+    return (time.perf_counter() - t0) * 1e3
+
+
 def _e2e(w, states, grads, flat, step_fn_of, stream, device, steps, t, barrier, reduce, ws, n_chunks=16,
          piece_bytes=128 << 20):
     """End to end through the C ABI with host buffers: every step copies all
@@ -778,6 +797,12 @@ def _e2e(w, states, grads, flat, step_fn_of, stream, device, steps, t, barrier, 
     t += 1
     one(t)                                   # warm-up
     torch.cuda.synchronize(device)
+    # the same copies with no compute, just before and just after the timed
+    # steps: the shared host link's concurrent rate varies over time on this
+    # pool (the same 2 x 16 GB took 101-159 ms a minute apart in one process)
+    piece = max(1, piece_bytes // 2)
+    link["both_full_ms_before"] = _both_full_ms(h_grad.view(torch.int16), f_grad.view(torch.int16), f_theta, h_out,
+                                                piece, s_in, s_out, device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     e0.record(stream)
@@ -787,6 +812,8 @@ def _e2e(w, states, grads, flat, step_fn_of, stream, device, steps, t, barrier, 
         one(t)
     e1.record(stream)
     torch.cuda.synchronize(device)
+    link["both_full_ms_after"] = _both_full_ms(h_grad.view(torch.int16), f_grad.view(torch.int16), f_theta, h_out,
+                                               piece, s_in, s_out, device)
     barrier()
     ms = reduce(e0.elapsed_time(e1), "max")
     return {"value": job_throughput(ws, w.numel, steps, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
