@@ -65,6 +65,8 @@ def parse_args(argv=None):
     p.add_argument("--traffic-command", default=None, help="the ncu command line, recorded with --record-traffic")
     p.add_argument("--grad-release", action="store_true",
                    help="time gradient release against a plain step() on --workload (GPT-2 small by default) and exit")
+    p.add_argument("--oracle-full-step", action="store_true",
+                   help="time the oracle over one step of the whole table (one-off measurement; prints one JSON line)")
     p.add_argument("--no-per-config", action="store_true",
                    help="skip timing the other workloads (flat 1M, GPT-2 small, ResNet-50, Lion 8B, stress set)")
     return p.parse_args(argv)
@@ -196,6 +198,60 @@ def cpu_baseline(w, rho_bits, seconds, grad_dtype="bf16"):
     s.close()
     return {"value": s.params * steps / dt, "unit": UNIT, "cores": s.threads, "kind": "oracle",
             "sample": f"{s.desc}; {steps} steps in {dt:.1f} s"}
+
+
+def oracle_full_step(args):
+    """The oracle over one AdamW step of every parameter of the workload (the
+    whole Llama-3.1-8B table by default), on the host cores: the inputs come
+    from the seeded device generators (copied to the host), the initial state
+    from the oracle's own split, and the step runs in 1M-element group-aligned
+    chunks on a thread per core. A measurement of the oracle as it stands, to
+    set beside the bounded sample that cpu_baseline times."""
+    import numpy as np
+    import torch
+    import oracle
+    from quantized_optimizer_state_gb300 import workloads as wl
+    w = _workload(args)
+    dev = torch.device("cuda", 0)
+    threads = _cpu_threads()
+    t0 = time.perf_counter()
+
+    def prepare(i):
+        p = w.params[i]
+        theta = wl.init_weight_device(p, i, dev).cpu().numpy()
+        g = wl.workload_grad_device(w, i, 1, dev, fp32=args.grad_dtype == "f32").cpu()
+        g = g.view(torch.int16).numpy().view(np.uint16) if args.grad_dtype != "f32" else g.numpy()
+        st = oracle.State.from_fp32(theta, args.rho_bits, w.optimizer == "adamw", w.hparams["weight_decay"])
+        return st, g
+
+    with cf.ThreadPoolExecutor(threads) as pool:
+        prepared = list(pool.map(prepare, range(len(w.params))))
+    setup = time.perf_counter() - t0
+    chunks = []
+    for st, g in prepared:
+        for lo in range(0, st.numel, 1 << 20):
+            hi = min(st.numel, lo + (1 << 20))
+            g0, g1 = lo // 32, (hi + 31) // 32
+            sub = oracle.State(st.theta_p[lo:hi], st.rho[lo:hi], st.m_q[lo:hi], st.m_scale[g0:g1],
+                               None if st.v_q is None else st.v_q[lo:hi],
+                               None if st.v_scale is None else st.v_scale[g0:g1], st.weight_decay, st.rho_bits)
+            chunks.append((sub, g[lo:hi]))
+    hp = w.hparams
+    if w.optimizer == "adamw":
+        f = lambda c: oracle.adamw_step([c[0]], [c[1]], hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], 1)
+    elif w.optimizer == "sgd":
+        f = lambda c: oracle.sgd_step([c[0]], [c[1]], hp["lr"], hp["momentum"])
+    else:
+        f = lambda c: oracle.lion_step([c[0]], [c[1]], hp["lr"], hp["beta1"], hp["beta2"])
+    with cf.ThreadPoolExecutor(threads) as pool:
+        t1 = time.perf_counter()
+        list(pool.map(f, chunks))
+        dt = time.perf_counter() - t1
+    out = {"oracle_full_step": {"workload": w.name, "params": w.numel, "tensors": len(w.params),
+                                "optimizer": w.optimizer, "step_seconds": dt, "params_per_s": w.numel / dt,
+                                "threads": threads, "chunks": len(chunks), "setup_seconds": setup}}
+    print(json.dumps(out), flush=True)
+    return 0
 
 
 def run_reference(args):
@@ -904,6 +960,8 @@ def main(argv=None):
         print(json.dumps(grad_release_study(args.workload if args.workload != "llama31_8b" else "gpt2_small")),
               flush=True)
         return 0
+    if args.oracle_full_step:
+        return oracle_full_step(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
