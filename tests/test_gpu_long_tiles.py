@@ -1,7 +1,8 @@
 """Parity of every step kernel, for the three tile lengths the library launches.
 
 Long tiles (8 chunks of 4096 elements) are used for tables large enough to
-give each resident CTA at least 8 of them (about 120M elements). Each long
+give each resident CTA at least 6 of them (up to about 120M elements, at 4
+resident CTAs per SM). Each long
 case is one row of 2^27 elements, checked against the oracle on chunks at its
 head, middle and tail over two steps (groups are independent, so a chunk's
 oracle step needs only that chunk's state). Short tiles (2 chunks) serve
