@@ -273,3 +273,20 @@ def test_verify_fast_arithmetic_argument_errors():
     A = 1 << 20
     assert _call("fo_verify_fast_arithmetic", None, None) == 1          # FO_ERR_NULL
     assert _call("fo_verify_fast_arithmetic", A + 4, None) == 2         # not 8-byte aligned
+
+
+def test_verify_binding_rejects_wrong_counts(monkeypatch):
+    """The counts buffer must be an int64 CUDA tensor of FO_VERIFY_COUNTS
+    entries on the current device: refused before any call otherwise."""
+    import torch
+    monkeypatch.setattr(fo, "_current_device", lambda: 0)
+    F = _FakeCuda
+    with pytest.raises(TypeError, match="counts"):
+        fo.fo_verify_fast_arithmetic(F(torch.int32, fo.FO_VERIFY_COUNTS))
+    with pytest.raises(ValueError, match="needs"):
+        fo.fo_verify_fast_arithmetic(F(torch.int64, fo.FO_VERIFY_COUNTS - 1))
+    with pytest.raises(ValueError, match="CUDA"):
+        fo.fo_verify_fast_arithmetic(torch.zeros(fo.FO_VERIFY_COUNTS, dtype=torch.int64))
+    assert len(fo.VERIFY_CHECKS) == fo.FO_VERIFY_COUNTS
+    hdr = open(os.path.join(ROOT, "include", "fo.h")).read()
+    assert re.search(r"#define FO_VERIFY_COUNTS (\d+)", hdr).group(1) == str(fo.FO_VERIFY_COUNTS)
