@@ -133,23 +133,47 @@ def _cpu_threads() -> int:
 
 
 class OracleSample:
-    """Host state of a few rows of the workload, cut into group-aligned chunks
-    that the oracle steps on parallel threads (the oracle itself is untouched)."""
+    """Host state of a few rows of the workload (or, with whole_table, of all of
+    them), cut into group-aligned chunks that the oracle steps on parallel
+    threads (the oracle itself is untouched). The sample's inputs come from the
+    host generators; the whole table's from the seeded device generators,
+    copied to the host (8e9 values would take minutes on the host)."""
 
-    def __init__(self, w, rho_bits, grad_dtype="bf16", chunk=1 << 20):
+    def __init__(self, w, rho_bits, grad_dtype="bf16", chunk=1 << 20, whole_table=False):
         import numpy as np
         import oracle
         from quantized_optimizer_state_gb300 import workloads as wl
         self.w = w
         names = {p.name: i for i, p in enumerate(w.params)}
-        rows = [names[n] for n in CPU_SAMPLE_ROWS if n in names] or [0]
+        rows = list(range(len(w.params))) if whole_table else \
+            ([names[n] for n in CPU_SAMPLE_ROWS if n in names] or [0])
         self.states, self.grads, self.chunks = [], [], []
         with_v = w.optimizer == "adamw"
-        for i in rows:
+        self.threads = _cpu_threads()
+
+        def host_inputs(i):
             p = w.params[i]
-            st = oracle.State.from_fp32(wl.init_weight(p, i), rho_bits, with_v,
-                                        w.hparams["weight_decay"])
             g = (wl.workload_grad_fp32 if grad_dtype == "f32" else wl.workload_grad_bf16)(w, i, 1)
+            return wl.init_weight(p, i), g
+
+        def device_inputs(i):
+            import torch
+            dev = torch.device("cuda", torch.cuda.current_device())
+            theta = wl.init_weight_device(w.params[i], i, dev).cpu().numpy()
+            g = wl.workload_grad_device(w, i, 1, dev, fp32=grad_dtype == "f32").cpu()
+            g = g.numpy() if grad_dtype == "f32" else g.view(torch.int16).numpy().view(np.uint16)
+            return theta, g
+
+        def prepare(i):
+            theta, g = (device_inputs if whole_table else host_inputs)(i)
+            return oracle.State.from_fp32(theta, rho_bits, with_v, w.hparams["weight_decay"]), g
+
+        t0 = time.perf_counter()
+        with cf.ThreadPoolExecutor(self.threads) as pool:
+            prepared = list(pool.map(prepare, rows))
+        self.setup_seconds = time.perf_counter() - t0
+        for i, (st, g) in zip(rows, prepared):
+            p = w.params[i]
             self.states.append(st)
             self.grads.append(g)
             for lo in range(0, p.numel, chunk):
@@ -161,11 +185,14 @@ class OracleSample:
                                    st.weight_decay, rho_bits)
                 self.chunks.append((sub, np.ascontiguousarray(g[lo:hi])))
         self.params = sum(s.numel for s in self.states)
-        self.threads = _cpu_threads()
         self.pool = cf.ThreadPoolExecutor(self.threads)
-        self.desc = (f"{len(rows)} rows of layer 0 ({self.params} params: "
-                     + ", ".join(w.params[i].name.split('.')[-2] for i in rows)
-                     + f"), {len(self.chunks)} chunks on {self.threads} threads")
+        if whole_table:
+            self.desc = (f"the whole table ({len(rows)} rows, {self.params} params), {len(self.chunks)} chunks "
+                         f"on {self.threads} threads")
+        else:
+            self.desc = (f"{len(rows)} rows of layer 0 ({self.params} params: "
+                         + ", ".join(w.params[i].name.split('.')[-2] for i in rows)
+                         + f"), {len(self.chunks)} chunks on {self.threads} threads")
 
     def step(self, t):
         import oracle
@@ -201,55 +228,20 @@ def cpu_baseline(w, rho_bits, seconds, grad_dtype="bf16"):
 
 
 def oracle_full_step(args):
-    """The oracle over one AdamW step of every parameter of the workload (the
-    whole Llama-3.1-8B table by default), on the host cores: the inputs come
-    from the seeded device generators (copied to the host), the initial state
-    from the oracle's own split, and the step runs in 1M-element group-aligned
-    chunks on a thread per core. A measurement of the oracle as it stands, to
-    set beside the bounded sample that cpu_baseline times."""
-    import numpy as np
-    import torch
-    import oracle
-    from quantized_optimizer_state_gb300 import workloads as wl
+    """The cpu_baseline leg with the whole table as its sample: the oracle over
+    one step of every parameter of the workload (all of Llama-3.1-8B by
+    default) on the host cores. A one-off measurement beside the bounded
+    sample that the default line reports."""
     w = _workload(args)
-    dev = torch.device("cuda", 0)
-    threads = _cpu_threads()
+    s = OracleSample(w, args.rho_bits, args.grad_dtype, whole_table=True)
     t0 = time.perf_counter()
-
-    def prepare(i):
-        p = w.params[i]
-        theta = wl.init_weight_device(p, i, dev).cpu().numpy()
-        g = wl.workload_grad_device(w, i, 1, dev, fp32=args.grad_dtype == "f32").cpu()
-        g = g.view(torch.int16).numpy().view(np.uint16) if args.grad_dtype != "f32" else g.numpy()
-        st = oracle.State.from_fp32(theta, args.rho_bits, w.optimizer == "adamw", w.hparams["weight_decay"])
-        return st, g
-
-    with cf.ThreadPoolExecutor(threads) as pool:
-        prepared = list(pool.map(prepare, range(len(w.params))))
-    setup = time.perf_counter() - t0
-    chunks = []
-    for st, g in prepared:
-        for lo in range(0, st.numel, 1 << 20):
-            hi = min(st.numel, lo + (1 << 20))
-            g0, g1 = lo // 32, (hi + 31) // 32
-            sub = oracle.State(st.theta_p[lo:hi], st.rho[lo:hi], st.m_q[lo:hi], st.m_scale[g0:g1],
-                               None if st.v_q is None else st.v_q[lo:hi],
-                               None if st.v_scale is None else st.v_scale[g0:g1], st.weight_decay, st.rho_bits)
-            chunks.append((sub, g[lo:hi]))
-    hp = w.hparams
-    if w.optimizer == "adamw":
-        f = lambda c: oracle.adamw_step([c[0]], [c[1]], hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], 1)
-    elif w.optimizer == "sgd":
-        f = lambda c: oracle.sgd_step([c[0]], [c[1]], hp["lr"], hp["momentum"])
-    else:
-        f = lambda c: oracle.lion_step([c[0]], [c[1]], hp["lr"], hp["beta1"], hp["beta2"])
-    with cf.ThreadPoolExecutor(threads) as pool:
-        t1 = time.perf_counter()
-        list(pool.map(f, chunks))
-        dt = time.perf_counter() - t1
-    out = {"oracle_full_step": {"workload": w.name, "params": w.numel, "tensors": len(w.params),
-                                "optimizer": w.optimizer, "step_seconds": dt, "params_per_s": w.numel / dt,
-                                "threads": threads, "chunks": len(chunks), "setup_seconds": setup}}
+    s.step(1)
+    dt = time.perf_counter() - t0
+    s.close()
+    out = {"oracle_full_step": {"workload": w.name, "params": s.params, "tensors": len(s.states),
+                                "optimizer": w.optimizer, "step_seconds": dt, "params_per_s": s.params / dt,
+                                "threads": s.threads, "chunks": len(s.chunks), "setup_seconds": s.setup_seconds,
+                                "sample": s.desc}}
     print(json.dumps(out), flush=True)
     return 0
 
