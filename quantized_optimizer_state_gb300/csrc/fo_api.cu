@@ -202,7 +202,8 @@ fo_status_t run_table(Opt opt, const fo_tensor_t *table, int32_t ntensors, const
                 total += table[j].numel;
         if (total == 0)
             continue;
-        const int64_t ctas = (int64_t)fo::sm_count() * fo::step_ctas_per_sm(opt, rb, gdt == FO_GRAD_F32 ? 32 : 16);
+        const int64_t ctas =
+            (int64_t)fo::sm_count() * fo::step_ctas_per_sm(opt, rb, gdt == FO_GRAD_F32 ? 32 : 16, fo::kLongChunks);
         const int chunks = total / ((int64_t)fo::kStepChunk * fo::kLongChunks) >= ctas * fo::kMinTilesPerCta
                                ? fo::kLongChunks
                            : total / ((int64_t)fo::kStepChunk * fo::kShortChunks) >= ctas ? fo::kShortChunks

@@ -30,14 +30,17 @@ constexpr int kMinTilesPerCta = 6;   // 8 and 6 tie on the large tables; GPT-2 s
 enum class Opt : int { kAdamW = 0, kSgd = 1, kLion = 2 };
 
 // Resident CTAs per SM each step kernel is built for (256 threads each), by
-// measurement on the Llama-3.1-8B table. AdamW with 8-bit rho and BF16
-// gradients runs 4 (64 registers, a few bytes of spills: 16.7 against 17.5
-// ms at 3); with 16-bit rho or FP32 gradients, which hold 4 or 8 more words a
-// thread, 3 (80 registers: 18.4 against 18.9 ms at 4). SGD and Lion, with one
-// moment, run 4 (6 % faster on the Lion step than 3).
-constexpr int step_ctas_per_sm(Opt o, int rho_bits, int grad_bits)
+// measurement. AdamW with 8-bit rho and BF16 gradients runs 4 (64 registers,
+// a few bytes of spills: 16.7 against 17.5 ms at 3 on the Llama-3.1-8B
+// table); with 16-bit rho or FP32 gradients, which hold 4 or 8 more words a
+// thread, 3 (80 registers: 18.4 against 18.9 ms at 4). Lion runs 4 (6 %
+// faster on the Llama-3.1-8B step than 3; 5 was 1 % slower). SGD runs 4 on
+// long tiles and 5 (48 registers) on short and one-chunk tiles, where its
+// tables are small and latency-bound (ResNet-50: 0.0524 against 0.0533 ms).
+constexpr int step_ctas_per_sm(Opt o, int rho_bits, int grad_bits, int chunks)
 {
-    return o != Opt::kAdamW ? 4 : (rho_bits == 8 && grad_bits == 16 ? 4 : 3);
+    return o == Opt::kSgd ? (chunks == kLongChunks ? 4 : 5)
+                          : o == Opt::kLion ? 4 : (rho_bits == 8 && grad_bits == 16 ? 4 : 3);
 }
 
 // One table row as the step kernel sees it. `coef` is the per-tensor scalar:

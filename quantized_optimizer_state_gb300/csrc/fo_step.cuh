@@ -8,12 +8,14 @@
 // group, so it is bound by HBM traffic and instruction issue, never by tensor
 // cores. A persistent grid (SMs x resident CTAs) walks the tiles of the
 // concatenated tensor list in a static round-robin. A tile is 8 (large
-// tables) or 2 (small ones) consecutive 4096-element chunks of one tensor,
-// stepped one after the other. In a chunk, a thread owns 16 contiguous
+// tables), 2 (small ones) or 1 (a few million elements) consecutive
+// 4096-element chunks of one tensor, stepped one after the other. In a chunk, a thread owns 16 contiguous
 // elements (half a group) and loads them with 128-bit streaming loads; the
 // two threads of a group combine their absmax with one shuffle, and the
 // results leave with 128-bit streaming stores. Pairs of elements are computed
-// with packed FP32 instructions and validated fast division and square root.
+// with packed FP32 instructions and exact fast division and square root
+// (fo_pair.cuh; their hardware-dependent domains are enumerated on the device
+// by fo_verify_fast_arithmetic).
 // Exact zeros (zero gradients, momenta and second moments, as in rows that
 // receive no gradient) stay on this path; a thread whose operands leave the
 // validated ranges (a zero theta', a tiny non-zero gradient, extreme
@@ -501,7 +503,7 @@ __device__ __forceinline__ int chunk_count(const StepRow &row, int64_t i0)
 
 // One thread's 16 elements of a tile, from data already loaded into L.
 // VNZ (AdamW): requantize v with no code 0 in groups with a non-zero scale.
-template <Opt O, int RB, int GB, bool VNZ>
+template <Opt O, int RB, int GB, bool VNZ, int CH>
 __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalars &s, int64_t i0, int cnt,
                                             Loaded &L)
 {
@@ -523,10 +525,11 @@ __device__ __forceinline__ void thread_step(const StepRow &row, const StepScalar
     const float cm = div_by_const(scale_value(L.ms), -127.0f, kRcp127);
     const float cv = WithV ? div_by_const(scale_value(L.vs), -255.0f, kRcp255) : 0.0f;
 
-    // AdamW re-splits theta on the fast path as soon as a quad is stepped (the
-    // 16 new theta values are never held: measured 5 % faster at 4 CTAs per
-    // SM); SGD and Lion re-split after the step (faster for them)
-    constexpr bool ES = (O == Opt::kAdamW);
+    // AdamW, and SGD on short tiles (5 CTAs per SM), re-split theta on the
+    // fast path as soon as a quad is stepped, so that the 16 new theta values
+    // are never held (AdamW at 4 CTAs: 5 % faster); SGD on long tiles and Lion
+    // re-split after the step (faster for them)
+    constexpr bool ES = (O == Opt::kAdamW) || (O == Opt::kSgd && CH != kLongChunks);
     float th[kEPT], z[kEPT], nr[kEPT];
     uint32_t tp[8], ro[8];
     float av = 0.0f;   // the thread's largest sqrt(v) (AdamW)
@@ -752,7 +755,7 @@ __device__ __forceinline__ void step_tiles(const StepParams &p, const StepScalar
                 break;
             Loaded L;
             load_chunk<RB, WithV, GB>(r, i0, cnt, L);
-            thread_step<O, RB, GB, VNZ>(r, s, i0, cnt, L);
+            thread_step<O, RB, GB, VNZ, CH>(r, s, i0, cnt, L);
         }
     }
 }
@@ -762,7 +765,7 @@ __device__ __forceinline__ void step_tiles(const StepParams &p, const StepScalar
 // from device memory when the kernel runs and the step scalars are derived
 // from it, once per CTA, into shared memory.
 template <Opt O, int RB, int GB, bool VNZ, int CH, bool DEV = false>
-__global__ void __launch_bounds__(kStepThreads, step_ctas_per_sm(O, RB, GB))
+__global__ void __launch_bounds__(kStepThreads, step_ctas_per_sm(O, RB, GB, CH))
 fo_fused_step_kernel(const __grid_constant__ StepParams p)
 {
     if constexpr (DEV) {
