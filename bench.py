@@ -65,6 +65,8 @@ def parse_args(argv=None):
     p.add_argument("--traffic-command", default=None, help="the ncu command line, recorded with --record-traffic")
     p.add_argument("--grad-release", action="store_true",
                    help="time gradient release against a plain step() on --workload (GPT-2 small by default) and exit")
+    p.add_argument("--grad-release-gemm-tokens", type=int, default=0,
+                   help="--grad-release with a GEMM backward over this many tokens per matrix parameter")
     p.add_argument("--oracle-full-step", action="store_true",
                    help="time the oracle over one step of the whole table (one-off measurement; prints one JSON line)")
     p.add_argument("--no-per-config", action="store_true",
@@ -875,33 +877,49 @@ def _e2e(w, states, grads, flat, step_fn_of, stream, device, steps, t, barrier, 
 # Gradient release against a plain optimizer step (drop-in optimizers)
 # ---------------------------------------------------------------------------
 
-def grad_release_study(name="gpt2_small", iters=20, warmup=5):
+def grad_release_study(name="gpt2_small", iters=20, warmup=5, gemm_tokens=0):
     """Backward + FlashAdamW step of a table's parameters three ways: a plain
     step() after backward, gradient release in buckets (the default size) and
-    release of every parameter on its own. The backward pass is synthetic (the
-    loss is sum(p * c) for a fixed random c per parameter, so each gradient is
-    c in BF16), identical in all three. Reported per iteration: the whole
-    iteration (host wall time), the host time spent in the optimizer's
-    stepping code, the GPU time of the optimizer's work (CUDA events around
-    each of its calls) and its kernel launches."""
+    release of every parameter on its own. The backward pass is synthetic and
+    identical in all three: the loss is sum(p * c) for a fixed random c per
+    parameter (each gradient is c in BF16), or, with gemm_tokens = T > 0, for
+    each matrix parameter p of shape (a, b) sum(x @ p) for a fixed random x of
+    shape (T, a), so that forward and backward are GEMMs of 2abT flops each,
+    as in a layer fed T tokens (a GPU-bound backward). Reported per
+    iteration: the whole iteration (host wall time), the host time spent in
+    the optimizer's stepping code, the GPU time of the optimizer's work (CUDA
+    events around each of its calls) and its kernel launches."""
     import torch
     from quantized_optimizer_state_gb300 import fo, optim
     from quantized_optimizer_state_gb300 import workloads as wl
     w = wl.workload(name)
     dev = torch.device("cuda", torch.cuda.current_device())
 
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+
     def make():
         ps, cs = [], []
         for i, p in enumerate(w.params):
             x = wl.init_weight_device(p, i, dev).view(p.shape)
             ps.append(torch.nn.Parameter(x))
-            cs.append(wl.workload_grad_device(w, i, 1, dev).view(p.shape))
+            if gemm_tokens and len(p.shape) == 2:
+                cs.append(torch.randn(gemm_tokens, p.shape[0], device=dev, generator=gen) * 0.01)
+            else:
+                cs.append(wl.workload_grad_device(w, i, 1, dev).view(p.shape))
         opt = optim.FlashAdamW(ps, lr=w.hparams["lr"], betas=(w.hparams["beta1"], w.hparams["beta2"]),
                                eps=w.hparams["eps"], weight_decay=w.hparams["weight_decay"])
+        # the optimizer holds compressed parameters as their BF16 theta': the
+        # GEMM inputs take the parameters' type
+        cs = [c.to(p.dtype) if c.shape != p.shape else c for p, c in zip(ps, cs)]
         return ps, cs, opt
 
+    def term(p, c):
+        return (c @ p).float().sum() if c.shape != p.shape else (p * c).float().sum()
+
     out = {"study": "grad_release", "workload": name, "params": w.numel, "tensors": len(w.params),
-           "iters": iters}
+           "iters": iters,
+           "backward": f"GEMMs over {gemm_tokens} tokens per matrix" if gemm_tokens else "element-wise"}
     for mode, bucket in (("plain_step", None), ("release_bucketed", 1 << 24), ("release_per_parameter", 0)):
         ps, cs, opt = make()
         calls = []                      # (host seconds, start event, end event) per optimizer call
@@ -919,7 +937,7 @@ def grad_release_study(name="gpt2_small", iters=20, warmup=5):
             opt.attach_grad_release(bucket_numel=bucket)
 
         def one():
-            sum((p * c).float().sum() for p, c in zip(ps, cs)).backward()
+            sum(term(p, c) for p, c in zip(ps, cs)).backward()
             if bucket is None:
                 opt.step()
                 opt.zero_grad(set_to_none=True)
@@ -949,8 +967,8 @@ def main(argv=None):
     if args.record_traffic:
         return record_traffic(args)
     if args.grad_release:
-        print(json.dumps(grad_release_study(args.workload if args.workload != "llama31_8b" else "gpt2_small")),
-              flush=True)
+        print(json.dumps(grad_release_study(args.workload if args.workload != "llama31_8b" else "gpt2_small",
+                                            gemm_tokens=args.grad_release_gemm_tokens)), flush=True)
         return 0
     if args.oracle_full_step:
         return oracle_full_step(args)
