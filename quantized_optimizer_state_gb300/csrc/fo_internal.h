@@ -33,14 +33,17 @@ enum class Opt : int { kAdamW = 0, kSgd = 1, kLion = 2 };
 // measurement. AdamW with 8-bit rho and BF16 gradients runs 4 (64 registers,
 // a few bytes of spills: 16.7 against 17.5 ms at 3 on the Llama-3.1-8B
 // table); with 16-bit rho or FP32 gradients, which hold 4 or 8 more words a
-// thread, 3 (80 registers: 18.4 against 18.9 ms at 4). Lion runs 4 (6 %
-// faster on the Llama-3.1-8B step than 3; 5 was 1 % slower). SGD runs 4 on
-// long tiles and 5 (48 registers) on short and one-chunk tiles, where its
-// tables are small and latency-bound (ResNet-50: 0.0524 against 0.0533 ms).
+// thread, 3 on long tiles (80 registers: 18.4 against 18.9 ms at 4 on the 8B
+// table) and 4 on the short and one-chunk tiles of small tables, which are
+// latency-bound (the 64M-element stress set at 16-bit rho: 0.165 against
+// 0.168 ms). Lion runs 4 (6 % faster on the Llama-3.1-8B step than 3; 5 was
+// 1 % slower). SGD runs 4 on long tiles and 5 (48 registers) on short and
+// one-chunk tiles (ResNet-50: 0.0524 against 0.0533 ms).
 constexpr int step_ctas_per_sm(Opt o, int rho_bits, int grad_bits, int chunks)
 {
-    return o == Opt::kSgd ? (chunks == kLongChunks ? 4 : 5)
-                          : o == Opt::kLion ? 4 : (rho_bits == 8 && grad_bits == 16 ? 4 : 3);
+    return o == Opt::kSgd    ? (chunks == kLongChunks ? 4 : 5)
+           : o == Opt::kLion ? 4
+                             : ((rho_bits == 8 && grad_bits == 16) || chunks != kLongChunks ? 4 : 3);
 }
 
 // One table row as the step kernel sees it. `coef` is the per-tensor scalar:
